@@ -1,0 +1,269 @@
+"""Plain fp64 CPU oracle for paged two-family QKV prep and paged attention.
+
+TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
+benchmark's CPU-baseline leg may import this module. The product path (the
+CUDA library and its Python binding) never calls it, and this module imports
+nothing from the product package.
+
+Everything is evaluated in float64 from the bf16 inputs; results are rounded to
+bf16 only by ``f64_to_bf16`` when a caller compares them with bf16 outputs.
+Each function states the passage it follows. The pages are three web pages of
+one inference-engine project:
+
+* "feat(kernels): Rust wrapper for the hd256 windowed paged prefill"
+  (Description): attention reads a paged pool, ``sm_scale`` is explicit and
+  unscaled attention uses 1.0, ``window_left`` has an inclusive-distance
+  contract, GQA maps query heads to KV heads by integer division.
+* "gemma4: serving prep needs pool-write forms" (Description, Proposed Plan):
+  Q is RMS-normed and rotated into a contiguous buffer; K is normed and rotated
+  and V weightless-normed, never rotated, straight into the layer's pool blocks;
+  for head_dim 512, V is the weightless norm of the same raw K sharing its
+  inverse RMS; the slot of token t is ``start_pos + t``.
+* "feat(gemma4): paged KV serving across both attention families"
+  (Description): local layers hd256 with 8 KV heads under a sliding window,
+  global layers hd512 with 1 KV head under full attention; decode runs the
+  prefill entry with one token.
+
+Readings where the pages are silent (each listed in the design notes):
+RMSNorm is ``x / sqrt(mean(x^2) + eps) * w`` with ``w`` a direct multiplier;
+norm, then weight, then rotary; rotary pairs element ``i`` with ``i + D/2``
+(half-split) over the full head dim with frequency ``theta^(-2i/D)``; the pool
+is ``[layer][page][K=0,V=1][kv_head][slot][D]``; key ``j`` is visible from
+query position ``p`` iff ``j <= p`` and (``window_left < 0`` or
+``p - j <= window_left``).
+
+Row chunking in ``attention`` only bounds memory: every output row is the
+plain definition evaluated on its own.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
+# --------------------------------------------------------------------------------------
+# bf16 <-> fp64
+# --------------------------------------------------------------------------------------
+def bf16_to_f64(bits) -> np.ndarray:
+    """Exact value of bf16 bit patterns (uint16) as float64."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(x) -> np.ndarray:
+    """Round float64 values directly to bfloat16, nearest with ties to even.
+
+    bf16 keeps 8 significant bits: for ``|x| = m * 2^e`` with ``0.5 <= m < 1``
+    the spacing of representable values is ``2^(e-8)``, floored at the
+    smallest subnormal ``2^-133``. ``np.rint`` rounds halves to even.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    finite = np.isfinite(x)
+    xf = np.where(finite, x, 0.0)
+    _, e = np.frexp(xf)
+    sp = np.maximum(e - 8, -133)
+    q = np.ldexp(np.rint(np.ldexp(xf, -sp)), sp)
+    over = np.abs(q) > BF16_MAX
+    q = np.where(over, np.copysign(np.inf, xf), q)
+    q = np.where(finite, q, x)
+    with np.errstate(over="ignore"):
+        f = q.astype(np.float32)
+    bits = (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    bits = np.where(np.isnan(x), np.uint16(0x7FC0), bits)
+    return bits.astype(np.uint16)
+
+
+# --------------------------------------------------------------------------------------
+# RMSNorm and rotary embedding
+# --------------------------------------------------------------------------------------
+def inv_rms(x: np.ndarray, eps: float) -> np.ndarray:
+    """1 / sqrt(mean(x^2) + eps) over the last axis (per token, per head).
+
+    "serving prep needs pool-write forms", Description: the hd512 V block
+    shares this denominator with K.
+    """
+    return 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def rope_cos_sin(positions, head_dim: int, theta: float):
+    """cos and sin of ``pos * theta^(-2i/D)`` for i in [0, D/2), in fp64."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    inv_freq = float(theta) ** (-2.0 * i / head_dim)
+    ang = np.asarray(positions, dtype=np.float64)[..., None] * inv_freq
+    return np.cos(ang), np.sin(ang)
+
+
+def rope_half_split(y: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
+    """Rotate pairs (y[i], y[i + D/2]) by the angle whose cos/sin are given."""
+    h = y.shape[-1] // 2
+    a, b = y[..., :h], y[..., h:]
+    return np.concatenate([a * cos - b * sin, b * cos + a * sin], axis=-1)
+
+
+# --------------------------------------------------------------------------------------
+# Positions and the slot contract
+# --------------------------------------------------------------------------------------
+def token_request_and_position(qo_indptr, start_pos):
+    """Request index and absolute position of every token of a ragged batch.
+
+    "serving prep needs pool-write forms", Proposed Plan: slot positions
+    derive from ``start_pos + token``.
+    """
+    qo_indptr = np.asarray(qo_indptr, dtype=np.int64)
+    start_pos = np.asarray(start_pos, dtype=np.int64)
+    lens = np.diff(qo_indptr)
+    req = np.repeat(np.arange(len(lens), dtype=np.int64), lens)
+    local = np.arange(int(qo_indptr[-1]), dtype=np.int64) - qo_indptr[req]
+    return req, start_pos[req] + local
+
+
+def slot_of(req, pos, kv_page_indptr, page_ids, page_size: int):
+    """(physical page id, in-page slot) holding KV position ``pos`` of ``req``."""
+    kv_page_indptr = np.asarray(kv_page_indptr, dtype=np.int64)
+    page_ids = np.asarray(page_ids, dtype=np.int64)
+    req = np.asarray(req, dtype=np.int64)
+    pos = np.asarray(pos, dtype=np.int64)
+    return page_ids[kv_page_indptr[req] + pos // page_size], pos % page_size
+
+
+def pool_row_offset(layer, page, kv, head, slot, num_pages: int, num_kv_heads: int,
+                    page_size: int, head_dim: int):
+    """Element offset of one head row in a dense [L][P][2][Hkv][ps][D] pool."""
+    return ((((np.asarray(layer, np.int64) * num_pages + page) * 2 + kv) * num_kv_heads
+             + head) * page_size + slot) * head_dim
+
+
+# --------------------------------------------------------------------------------------
+# Prep: norm + rotary, K/V into the pool
+# --------------------------------------------------------------------------------------
+def prep_hd256(q_raw, k_raw, v_raw, w_q, w_k, eps, positions, theta):
+    """hd256 serving prep ("serving prep needs pool-write forms", Proposed Plan,
+    first item): q = rope(norm_wq(q)), k = rope(norm_wk(k)), v = norm(v) unrotated.
+
+    Arrays are fp64: q_raw [T, Hq, D], k_raw/v_raw [T, Hkv, D], w [D].
+    Returns (q_out, k, v) in fp64.
+    """
+    D = q_raw.shape[-1]
+    c, s = rope_cos_sin(positions, D, theta)
+    c, s = c[:, None, :], s[:, None, :]
+    q = rope_half_split(q_raw * inv_rms(q_raw, eps) * w_q, c, s)
+    k = rope_half_split(k_raw * inv_rms(k_raw, eps) * w_k, c, s)
+    v = v_raw * inv_rms(v_raw, eps)
+    return q, k, v
+
+
+def prep_hd512(q_raw, k_raw, w_q, w_k, eps, positions, theta):
+    """hd512 serving prep ("serving prep needs pool-write forms", Proposed Plan,
+    second item): k = rope(norm_wk(k_raw)); v = k_raw * inv_rms(k_raw), the
+    weightless norm of the same raw K with the same denominator, unrotated.
+    Q is normed and rotated like the hd256 form.
+    """
+    D = q_raw.shape[-1]
+    c, s = rope_cos_sin(positions, D, theta)
+    c, s = c[:, None, :], s[:, None, :]
+    q = rope_half_split(q_raw * inv_rms(q_raw, eps) * w_q, c, s)
+    r_k = inv_rms(k_raw, eps)
+    k = rope_half_split(k_raw * r_k * w_k, c, s)
+    v = k_raw * r_k
+    return q, k, v
+
+
+def prep_pool_writes(req, pos, kv_page_indptr, page_ids, page_size, layer, num_pages,
+                     num_kv_heads, head_dim):
+    """Element offsets [T, 2, Hkv] of the K and V rows each token writes."""
+    page, slot = slot_of(req, pos, kv_page_indptr, page_ids, page_size)
+    kv = np.arange(2, dtype=np.int64)[None, :, None]
+    head = np.arange(num_kv_heads, dtype=np.int64)[None, None, :]
+    return pool_row_offset(layer, page[:, None, None], kv, head, slot[:, None, None],
+                           num_pages, num_kv_heads, page_size, head_dim)
+
+
+# --------------------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------------------
+def visible(p, j, window_left: int):
+    """Causal mask with the inclusive-distance window ("Rust wrapper for the
+    hd256 windowed paged prefill", Description): key j is visible from query
+    position p iff j <= p and (window_left < 0 or p - j <= window_left)."""
+    p = np.asarray(p)
+    j = np.asarray(j)
+    m = j <= p
+    if window_left >= 0:
+        m = m & (p - j <= window_left)
+    return m
+
+
+def gather_kv(pool_bits: np.ndarray, layer: int, pages_of_req, kv_len: int, page_size: int):
+    """K and V of positions [0, kv_len) of one request, fp64 [kv_len, Hkv, D] each."""
+    j = np.arange(kv_len, dtype=np.int64)
+    pages = np.asarray(pages_of_req, dtype=np.int64)[j // page_size]
+    slots = j % page_size
+    k = bf16_to_f64(pool_bits[layer, pages, 0, :, slots, :])
+    v = bf16_to_f64(pool_bits[layer, pages, 1, :, slots, :])
+    return k, v
+
+
+def attend_rows(q_rows, p_rows, k, v, window_left: int, sm_scale: float):
+    """Masked softmax attention of query rows q_rows [n, D] at positions p_rows
+    over keys k [kv, D] and values v [kv, D]: o = sum_j softmax_j(s) v_j with
+    s_j = sm_scale * <q, k_j> over the visible j."""
+    s = sm_scale * (q_rows @ k.T)
+    mask = visible(np.asarray(p_rows)[:, None], np.arange(k.shape[0])[None, :], window_left)
+    s = np.where(mask, s, -np.inf)
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.where(mask, np.exp(s - m), 0.0)
+    return (e @ v) / np.sum(e, axis=1, keepdims=True)
+
+
+def attention(q_bits, pool_bits, layer: int, qo_indptr, kv_page_indptr, page_ids,
+              last_page_len, start_pos, num_kv_heads: int, window_left: int,
+              sm_scale: float, rows=None, row_chunk: int = 512):
+    """Paged prefill attention over a page table (fp64).
+
+    q_bits: bf16 bits [T, Hq, D]; pool_bits: bf16 bits [L, P, 2, Hkv, ps, D].
+    The kv length of request r is (pages_r - 1) * ps + last_page_len_r, and its
+    queries sit at positions start_pos_r + t. Query head h reads KV head
+    h // (Hq / Hkv). ``rows``: optional int array [n, 2] of (token, head) to
+    evaluate; returns fp64 [n, D]. Without it returns fp64 [T, Hq, D].
+    """
+    qo_indptr = np.asarray(qo_indptr, dtype=np.int64)
+    kv_page_indptr = np.asarray(kv_page_indptr, dtype=np.int64)
+    page_ids = np.asarray(page_ids, dtype=np.int64)
+    last_page_len = np.asarray(last_page_len, dtype=np.int64)
+    T, Hq, D = q_bits.shape
+    ps = pool_bits.shape[4]
+    group = Hq // num_kv_heads
+    req_of, pos_of = token_request_and_position(qo_indptr, start_pos)
+    if rows is None:
+        tt, hh = np.meshgrid(np.arange(T), np.arange(Hq), indexing="ij")
+        sel = np.stack([tt.ravel(), hh.ravel()], axis=1)
+    else:
+        sel = np.asarray(rows, dtype=np.int64).reshape(-1, 2)
+    out = np.zeros((len(sel), D), dtype=np.float64)
+    sel_req = req_of[sel[:, 0]] if len(sel) else np.zeros(0, np.int64)
+    for r in np.unique(sel_req):
+        npages = kv_page_indptr[r + 1] - kv_page_indptr[r]
+        kv_len = int((npages - 1) * ps + last_page_len[r])
+        k, v = gather_kv(pool_bits, layer, page_ids[kv_page_indptr[r]:kv_page_indptr[r + 1]],
+                         kv_len, ps)
+        idx_r = np.nonzero(sel_req == r)[0]
+        for g in range(num_kv_heads):
+            idx = idx_r[(sel[idx_r, 1] // group) == g]
+            for c in range(0, len(idx), row_chunk):
+                ii = idx[c:c + row_chunk]
+                qr = bf16_to_f64(q_bits[sel[ii, 0], sel[ii, 1], :])
+                out[ii] = attend_rows(qr, pos_of[sel[ii, 0]], k[:, g, :], v[:, g, :],
+                                      window_left, sm_scale)
+    if rows is None:
+        return out.reshape(T, Hq, D)
+    return out
+
+
+def visible_pairs(qo_indptr, start_pos, window_left: int) -> int:
+    """Number of (query, key) pairs the mask keeps, per query head."""
+    _, pos = token_request_and_position(qo_indptr, start_pos)
+    n = pos + 1
+    if window_left >= 0:
+        n = np.minimum(n, window_left + 1)
+    return int(n.sum())
