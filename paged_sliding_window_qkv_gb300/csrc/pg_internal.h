@@ -1,0 +1,85 @@
+// Internal declarations shared by the library's host code and kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace pg {
+
+// Device view of a plan's metadata (all int32, uploaded by the plan builder).
+struct PlanDev {
+  const int32_t* qo_indptr;       // [R+1]
+  const int32_t* kv_page_indptr;  // [R+1]
+  const int32_t* page_ids;        // [num_page_ids]
+  const int32_t* last_page_len;   // [R]
+  const int32_t* start_pos;       // [R]
+  const int32_t* tok_req;         // [T]   request of each token row
+  const int32_t* work_req;        // [num_work] prefill work item: request
+  const int32_t* work_tok0;       // [num_work] prefill work item: first request-local token
+  int32_t num_req, num_tokens, num_page_ids, num_work;
+};
+
+// Device view of one family's pool, already narrowed to the called layer.
+struct PoolDev {
+  __nv_bfloat16* layer_base;  // pool base + layer * stride_layer
+  int64_t stride_page, stride_kv, stride_head;  // elements; stride_slot == head_dim
+  int32_t num_pages, page_size, num_kv_heads, head_dim;
+};
+
+struct PrepArgs {
+  PlanDev plan;
+  PoolDev pool;
+  const __nv_bfloat16* q_raw;
+  const __nv_bfloat16* k_raw;
+  const __nv_bfloat16* v_raw;  // null for the head_dim-512 form
+  int64_t q_stride, k_stride, v_stride;  // token strides, elements
+  const __nv_bfloat16* w_q;
+  const __nv_bfloat16* w_k;
+  const float* rope_cos;
+  const float* rope_sin;
+  __nv_bfloat16* q_out;
+  float eps;
+  int32_t rope_rows;
+  int32_t num_qo_heads;
+  int* status;
+};
+
+struct AttnArgs {
+  PlanDev plan;
+  PoolDev pool;
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  float* ws_o;    // decode form: partial outputs [R][Hq][max_chunks][D]
+  float* ws_ml;   // decode form: [R][Hq][max_chunks][2] (running max in log2 units, sum)
+  float sm_scale_log2;  // sm_scale * log2(e)
+  int32_t window_left;
+  int32_t num_qo_heads;
+  int32_t group;        // Hq / Hkv
+  int32_t cta_tile_q;   // query tokens per prefill CTA
+  int32_t kv_chunk;     // keys per decode chunk
+  int32_t max_chunks;
+  int* status;
+};
+
+// Device status word: set by kernels that skip an out-of-range access.
+constexpr int kStatusBounds = 1;
+
+// Launch counter shared by all launchers.
+void count_launch();
+
+// ---- launchers (return cudaError_t of the launch) ----
+cudaError_t launch_rope_table(float* cos_t, float* sin_t, int32_t rows, int32_t head_dim,
+                              double theta, cudaStream_t stream);
+cudaError_t launch_prep_hd256(const PrepArgs& a, cudaStream_t stream);
+cudaError_t launch_prep_hd512(const PrepArgs& a, cudaStream_t stream);
+
+// Query tokens per CTA of the prefill attention kernel for this geometry, or 0 when the
+// kernel does not support it. Defined next to the kernels (the kernel's own derivation).
+int32_t attn_kernel_cta_tile_q(int32_t head_dim, int32_t group);
+// Keys per split-KV chunk of the decode kernel.
+int32_t attn_kernel_kv_chunk(int32_t head_dim);
+cudaError_t launch_attn_prefill(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);
+cudaError_t launch_attn_decode(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);
+
+}  // namespace pg

@@ -1,0 +1,246 @@
+"""ctypes binding of ``libpg.so`` (declared in ``include/pg.h``).
+
+Argument marshalling only: every step of the path runs in the library's
+kernels. Device buffers are passed as torch CUDA tensors (their ``data_ptr``),
+host plan inputs as numpy arrays, streams as ``torch.cuda.Stream`` (default:
+torch's current stream). Each ``pg_*`` function returns the library's status
+code; ``check`` turns a nonzero code into ``PgError``.
+
+Importing this module loads the library and raises ``ImportError`` if it has not
+been built: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpg.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python -c 'import __graft_entry__ as g; g.build()'`")
+_lib = C.CDLL(LIB_PATH)
+
+# status codes (include/pg.h)
+PG_OK = 0
+PG_ERR_ARG = -1
+PG_ERR_PAGE_OOB = -2
+PG_ERR_LAST_PAGE_LEN = -3
+PG_ERR_I32_OVERFLOW = -4
+PG_ERR_ZERO_KV_HEADS = -5
+PG_ERR_HEADS = -6
+PG_ERR_NONFINITE = -7
+PG_ERR_ROPE_RANGE = -8
+PG_ERR_COVERAGE = -9
+PG_ERR_LAYER = -10
+PG_ERR_LAYOUT = -11
+PG_ERR_PLAN_MISMATCH = -12
+PG_ERR_WINDOW = -13
+PG_ERR_WORKSPACE = -14
+PG_ERR_STREAM = -15
+PG_ERR_CUDA = -16
+PG_ERR_DEVICE_BOUNDS = -17
+PG_ERR_ALIGN = -18
+
+
+class PgError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {pg_status_string(status)} ({status})")
+
+
+class pg_pool_t(C.Structure):
+    _fields_ = [("base", C.c_void_p),
+                ("num_layers", C.c_int32), ("num_pages", C.c_int32), ("page_size", C.c_int32),
+                ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("stride_layer", C.c_int64), ("stride_page", C.c_int64), ("stride_kv", C.c_int64),
+                ("stride_head", C.c_int64), ("stride_slot", C.c_int64),
+                ("capacity", C.c_int64)]
+
+
+class pg_plan_info_t(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "num_req", "num_tokens", "num_qo_heads", "num_kv_heads", "head_dim", "page_size",
+        "max_page_id", "max_last_page_len", "max_qo_len", "max_kv_len", "max_pos_end",
+        "cta_tile_q", "decode", "kv_chunk", "max_chunks", "num_work")] + [
+        ("d_page_ids", C.c_void_p), ("stream", C.c_void_p)]
+
+
+_P = C.c_void_p
+_I32, _I64, _F32, _F64, _SZ = C.c_int32, C.c_int64, C.c_float, C.c_double, C.c_size_t
+
+
+def _sig(name, res, *args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = list(args)
+    return f
+
+
+_plan = _sig("pg_plan_paged_prefill", C.c_int, C.POINTER(_P), _I32, _P, _P, _P, _P, _P,
+             _I32, _I32, _I32, _I32, _P)
+_destroy = _sig("pg_plan_destroy", None, _P)
+_info = _sig("pg_plan_info", C.c_int, _P, C.POINTER(pg_plan_info_t))
+_rope = _sig("pg_rope_table", C.c_int, _P, _P, _I32, _I32, _F64, _P)
+_prep256 = _sig("pg_prep_paged_hd256", C.c_int, _P, C.POINTER(pg_pool_t), _I32,
+                _P, _I64, _P, _I64, _P, _I64, _P, _P, _F32, _P, _P, _I32, _P, _P)
+_prep512 = _sig("pg_prep_paged_hd512", C.c_int, _P, C.POINTER(pg_pool_t), _I32,
+                _P, _I64, _P, _I64, _P, _P, _F32, _P, _P, _I32, _P, _P)
+_wsb = _sig("pg_workspace_bytes", _SZ, _P)
+_attn256 = _sig("pg_attn_paged_prefill", C.c_int, _P, C.POINTER(pg_pool_t), _I32, _P, _P,
+                _I32, _F32, _P, _SZ, _P)
+_attn512 = _sig("pg_attn_paged_prefill_hd512", C.c_int, _P, C.POINTER(pg_pool_t), _I32, _P, _P,
+                _I32, _F32, _P, _SZ, _P)
+_devstat = _sig("pg_device_status", C.c_int, _P)
+_launches = _sig("pg_launch_count", _I64)
+_sstr = _sig("pg_status_string", C.c_char_p, C.c_int)
+
+
+# ------------------------------------------------------------------------------ helpers
+def _ptr(t) -> int | None:
+    """Device address of a torch tensor (None passes NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _host(a, dtype):
+    if a is None:
+        return None, None
+    arr = np.ascontiguousarray(np.asarray(a), dtype=dtype)
+    return arr, arr.ctypes.data
+
+
+def check(status: int, what: str = "pg call") -> None:
+    if status != PG_OK:
+        raise PgError(status, what)
+
+
+def pg_status_string(status: int) -> str:
+    return _sstr(int(status)).decode()
+
+
+def pg_launch_count() -> int:
+    return int(_launches())
+
+
+def pg_device_status(stream=None) -> int:
+    return _devstat(_stream(stream))
+
+
+# ------------------------------------------------------------------------------ plan
+class Plan:
+    """Owning handle of a ``pg_plan_t``; destroyed with the object or ``close()``."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+
+    def close(self):
+        if self.handle:
+            _destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def info(self) -> pg_plan_info_t:
+        i = pg_plan_info_t()
+        check(_info(self.handle, C.byref(i)), "pg_plan_info")
+        return i
+
+    @property
+    def _as_parameter_(self):
+        return self.handle
+
+
+def pg_plan_paged_prefill(plan, num_req, qo_indptr, kv_page_indptr, page_ids, last_page_len,
+                          start_pos, num_qo_heads, num_kv_heads, head_dim, page_size,
+                          stream=None):
+    """Build (plan=None) or update (plan=Plan) a plan. Returns (status, Plan or None)."""
+    h = _P(plan.handle if plan is not None else None)
+    keep = [_host(qo_indptr, np.int64), _host(kv_page_indptr, np.int64),
+            _host(page_ids, np.int32), _host(last_page_len, np.int32), _host(start_pos, np.int64)]
+    rc = _plan(C.byref(h), int(num_req), *[k[1] for k in keep], int(num_qo_heads),
+               int(num_kv_heads), int(head_dim), int(page_size), _stream(stream))
+    del keep
+    if plan is not None:
+        return rc, plan
+    return rc, (Plan(h.value) if rc == PG_OK else None)
+
+
+def pg_workspace_bytes(plan) -> int:
+    return int(_wsb(plan.handle if plan is not None else None))
+
+
+# ------------------------------------------------------------------------------ pool
+def pool_descriptor(pool, **override) -> pg_pool_t:
+    """pg_pool_t for a torch bf16 tensor shaped [L, P, 2, Hkv, ps, D] (strides taken from the
+    tensor, so a non-dense tensor is reported by the library, not hidden here)."""
+    L, P, two, Hkv, ps, D = pool.shape
+    st = pool.stride()
+    d = pg_pool_t(pool.data_ptr(), L, P, ps, Hkv, D, st[0], st[1], st[2], st[3], st[4],
+                  pool.numel())
+    for k, v in override.items():
+        setattr(d, k, v)
+    return d
+
+
+# ------------------------------------------------------------------------------ kernels
+def pg_rope_table(rope_cos, rope_sin, rows, head_dim, theta, stream=None) -> int:
+    return _rope(_ptr(rope_cos), _ptr(rope_sin), int(rows), int(head_dim), float(theta),
+                 _stream(stream))
+
+
+def pg_prep_paged_hd256(plan, pool: pg_pool_t, layer, q_raw, q_tok_stride, k_raw, k_tok_stride,
+                        v_raw, v_tok_stride, w_q, w_k, eps, rope_cos, rope_sin, rope_rows,
+                        q_out, stream=None) -> int:
+    return _prep256(plan.handle if plan is not None else None, C.byref(pool), int(layer),
+                    _ptr(q_raw), int(q_tok_stride), _ptr(k_raw), int(k_tok_stride), _ptr(v_raw),
+                    int(v_tok_stride), _ptr(w_q), _ptr(w_k), float(eps), _ptr(rope_cos),
+                    _ptr(rope_sin), int(rope_rows), _ptr(q_out), _stream(stream))
+
+
+def pg_prep_paged_hd512(plan, pool: pg_pool_t, layer, q_raw, q_tok_stride, k_raw, k_tok_stride,
+                        w_q, w_k, eps, rope_cos, rope_sin, rope_rows, q_out,
+                        stream=None) -> int:
+    return _prep512(plan.handle if plan is not None else None, C.byref(pool), int(layer),
+                    _ptr(q_raw), int(q_tok_stride), _ptr(k_raw), int(k_tok_stride), _ptr(w_q),
+                    _ptr(w_k), float(eps), _ptr(rope_cos), _ptr(rope_sin), int(rope_rows),
+                    _ptr(q_out), _stream(stream))
+
+
+def pg_attn_paged_prefill(plan, pool: pg_pool_t, layer, q, out, window_left, sm_scale,
+                          workspace=None, ws_bytes=0, stream=None) -> int:
+    return _attn256(plan.handle if plan is not None else None, C.byref(pool), int(layer), _ptr(q),
+                    _ptr(out), int(window_left), float(sm_scale), _ptr(workspace), int(ws_bytes),
+                    _stream(stream))
+
+
+def pg_attn_paged_prefill_hd512(plan, pool: pg_pool_t, layer, q, out, window_left, sm_scale,
+                                workspace=None, ws_bytes=0, stream=None) -> int:
+    return _attn512(plan.handle if plan is not None else None, C.byref(pool), int(layer), _ptr(q),
+                    _ptr(out), int(window_left), float(sm_scale), _ptr(workspace), int(ws_bytes),
+                    _stream(stream))
+
+
+EXPORTED = ["pg_plan_paged_prefill", "pg_plan_destroy", "pg_plan_info", "pg_rope_table",
+            "pg_prep_paged_hd256", "pg_prep_paged_hd512", "pg_workspace_bytes",
+            "pg_attn_paged_prefill", "pg_attn_paged_prefill_hd512", "pg_device_status",
+            "pg_launch_count", "pg_status_string"]

@@ -1,0 +1,81 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared symbol,
+and rejects bad plans before touching CUDA."""
+import os
+import re
+
+import pytest
+
+import rejects
+from paged_sliding_window_qkv_gb300 import pg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pg.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(pg_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["pg_plan_paged_prefill", "pg_prep_paged_hd256", "pg_prep_paged_hd512",
+                     "pg_attn_paged_prefill", "pg_attn_paged_prefill_hd512"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported():
+    for name in declared_functions():
+        assert hasattr(pg._lib, name), name
+
+
+def test_status_strings_are_distinct():
+    codes = [v for k, v in vars(pg).items() if k.startswith("PG_ERR_") or k == "PG_OK"]
+    texts = {pg.pg_status_string(c) for c in codes}
+    assert len(texts) == len(codes)
+    assert pg.pg_status_string(12345) == "unknown status"
+
+
+def _plan(a):
+    return pg.pg_plan_paged_prefill(None, a["num_req"], a["qo_indptr"], a["kv_page_indptr"],
+                                    a["page_ids"], a["last_page_len"], a["start_pos"],
+                                    a["num_qo_heads"], a["num_kv_heads"], a["head_dim"],
+                                    a["page_size"], stream=0)
+
+
+PLAN_CASES = [c for c in rejects.load_cases() if c[1] == "plan"]
+
+
+@pytest.mark.parametrize("name,stage,expected,source", PLAN_CASES, ids=[c[0] for c in PLAN_CASES])
+def test_pages_plan_rejects(name, stage, expected, source):
+    before = pg.pg_launch_count()
+    rc, plan = _plan(rejects.plan_case(name))
+    assert rc == getattr(pg, expected), (name, pg.pg_status_string(rc))
+    assert plan is None
+    assert pg.pg_launch_count() == before
+
+
+@pytest.mark.parametrize("name", sorted(rejects.PLAN_ONLY_EXTRA))
+def test_more_plan_rejects(name):
+    a, expected = rejects.plan_extra_case(name)
+    rc, plan = _plan(a)
+    assert rc == getattr(pg, expected), (name, pg.pg_status_string(rc))
+    assert plan is None
+
+
+def test_zero_kv_heads_wins_over_other_faults():
+    # the head relation is settled first, before anything could divide by it
+    a = rejects.plan_case("zero_kv_heads")
+    a["last_page_len"][0] = 999
+    a["num_qo_heads"] = 7
+    rc, _ = _plan(a)
+    assert rc == pg.PG_ERR_ZERO_KV_HEADS
+
+
+def test_null_plan_is_rejected_everywhere():
+    d = pg.pg_pool_t()
+    assert pg.pg_prep_paged_hd256(None, d, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1e-6, 0, 0, 1, 0, 0) == pg.PG_ERR_ARG
+    assert pg.pg_prep_paged_hd512(None, d, 0, 0, 0, 0, 0, 0, 0, 1e-6, 0, 0, 1, 0, 0) == pg.PG_ERR_ARG
+    assert pg.pg_attn_paged_prefill(None, d, 0, 0, 0, -1, 1.0, None, 0, 0) == pg.PG_ERR_ARG
+    assert pg.pg_attn_paged_prefill_hd512(None, d, 0, 0, 0, -1, 1.0, None, 0, 0) == pg.PG_ERR_ARG
+    assert pg.pg_workspace_bytes(None) == 0
+    assert pg.pg_rope_table(0, 0, 4, 256, 1e4, 0) == pg.PG_ERR_ARG
