@@ -135,12 +135,13 @@ def test_launch_rejects(name, stage, expected, source):
 
 def test_attention_rejects_bad_window_and_small_workspace():
     run = _base_run()
-    before = pg.pg_launch_count()
-    assert run.attn_status(window_left=-2) == pg.PG_ERR_WINDOW
     # a decode plan needs workspace
     fi = W.custom_family(W.HD512, np.ones(3, np.int64), [600, 3000, 9], seed=3, pool_fill="normal")
     dec = FamilyRun(fi)
     assert dec.ws_bytes > 0
+    torch.cuda.synchronize()
+    before = pg.pg_launch_count()
+    assert run.attn_status(window_left=-2) == pg.PG_ERR_WINDOW
     assert pg.pg_attn_paged_prefill_hd512(dec.plan, dec.pool_desc, 0, dec.q_raw, dec.out, -1, 1.0,
                                           dec.ws, dec.ws_bytes - 4) == pg.PG_ERR_WORKSPACE
     assert pg.pg_attn_paged_prefill_hd512(dec.plan, dec.pool_desc, 0, dec.q_raw, dec.out, -1, 1.0,
