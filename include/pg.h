@@ -225,6 +225,39 @@ int pg_attn_paged_prefill_hd512(const pg_plan_t plan, const pg_pool_t* pool, int
                                 float sm_scale, void* workspace, size_t ws_bytes,
                                 pg_stream_t stream);
 
+/* ---------------------------------------------------------------- decode without allocation */
+/*
+ * Bytes of library-owned device scratch behind pg_attn_paged_decode_noalloc. The buffer is a
+ * static device array of this size in the library image: every GPU that loads the library
+ * holds it from first use until the process exits.
+ */
+#define PG_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * pg_attn_paged_decode_noalloc -- the decode form of paged attention (a plan whose requests
+ * each have exactly one query token, head_dim 256 or 512) with its split-KV partials kept in
+ * the library's static scratch instead of a caller workspace. The pages have no counterpart
+ * for this entry: it exists for callers that cannot allocate device memory at call time
+ * (for example code running under an allocator that forbids cudaMalloc once serving has
+ * started, or a host runtime that owns all device memory and hands out only the tensors it
+ * manages). It computes exactly what pg_attn_paged_prefill / pg_attn_paged_prefill_hd512
+ * compute for the same decode plan and arguments, with the same checks and status codes.
+ *
+ * The call allocates nothing. On the first call on a device it looks up the device address
+ * of the static scratch (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture. Every call on a device shares the one scratch buffer and
+ * overwrites it: calls whose kernels overlap on the GPU (different streams, or several
+ * plans in flight at once) race on it, so serialise them. Nothing in the scratch needs to
+ * start at zero: each partial result the merge step reads is written by the same call.
+ *
+ * Errors: as pg_attn_paged_prefill, plus PG_ERR_PLAN_MISMATCH for a plan that is not a
+ * decode plan, PG_ERR_WORKSPACE when pg_workspace_bytes(plan) exceeds
+ * PG_NOALLOC_SCRATCH_BYTES, and PG_ERR_STREAM when the current device is not the plan's.
+ */
+int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, int32_t layer,
+                                 const pg_bf16_t* q, pg_bf16_t* out, int32_t window_left,
+                                 float sm_scale, pg_stream_t stream);
+
 /* ---------------------------------------------------------------- diagnostics */
 /* Synchronise `stream`, then read and clear the current device's status word.
  * Returns PG_OK, PG_ERR_DEVICE_BOUNDS (a kernel skipped an out-of-range access),

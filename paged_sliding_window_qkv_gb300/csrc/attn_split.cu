@@ -15,9 +15,12 @@
 //   chunk); each chunk writes a partial (o, m, l) and a merge kernel combines them.
 //   A request whose visible keys fit one chunk is written directly.
 #include "pg_internal.h"
+#include "../../include/pg.h"
 
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <mutex>
 
 namespace pg {
 namespace {
@@ -451,6 +454,38 @@ cudaError_t launch_attn_decode(const AttnArgs& a, int32_t head_dim, cudaStream_t
   else attn_merge_kernel<512><<<mgrid, 512 / 4, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+// Decode partials in library-owned scratch, for callers that cannot allocate device memory.
+// The array is part of the library image; host code may not use its name as an address, so
+// the device address is looked up once per device with cudaGetSymbolAddress.
+namespace {
+static __device__ __align__(256) unsigned char g_decode_scratch[PG_NOALLOC_SCRATCH_BYTES];
+std::mutex g_decode_scratch_mu;
+void* g_decode_scratch_addr[128] = {nullptr};
+}  // namespace
+
+cudaError_t launch_attn_decode_static(AttnArgs a, int32_t head_dim, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_decode_scratch_mu);
+    if (!g_decode_scratch_addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_decode_scratch);
+      if (e != cudaSuccess) return e;
+      g_decode_scratch_addr[dev] = p;
+    }
+    base = g_decode_scratch_addr[dev];
+  }
+  const size_t rows = (size_t)a.plan.num_req * a.num_qo_heads * a.max_chunks;
+  a.ws_o = reinterpret_cast<float*>(base);
+  a.ws_ml = a.ws_o + rows * (size_t)head_dim;
+  return launch_attn_decode(a, head_dim, stream);
 }
 
 }  // namespace pg

@@ -371,6 +371,18 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
   return e == cudaSuccess ? PG_OK : PG_ERR_CUDA;
 }
 
+// The device's status word if it already exists; never allocates.
+int* status_word_existing(int* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+    *err = PG_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  *err = g_status_dev[dev] ? PG_OK : PG_ERR_CUDA;
+  return g_status_dev[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -473,6 +485,51 @@ int pg_attn_paged_prefill_hd512(const pg_plan_t plan, const pg_pool_t* pool, int
                                 pg_stream_t stream) {
   return attn_common(plan, pool, layer, 512, q, out, window_left, sm_scale, workspace, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, int32_t layer,
+                                 const pg_bf16_t* q, pg_bf16_t* out, int32_t window_left,
+                                 float sm_scale, pg_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!plan) return PG_ERR_ARG;
+  if (s != plan->stream) return PG_ERR_STREAM;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PG_ERR_CUDA;
+  if (dev != plan->device) return PG_ERR_STREAM;
+  if (!plan->decode && plan->num_req > 0) return PG_ERR_PLAN_MISMATCH;
+  if (workspace_bytes(plan) > PG_NOALLOC_SCRATCH_BYTES) return PG_ERR_WORKSPACE;
+  const int32_t D = plan->head_dim;
+  if (D != 256 && D != 512) return PG_ERR_PLAN_MISMATCH;
+  int rc = check_plan_pool(plan, pool, layer, D);
+  if (rc) return rc;
+  const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
+  const int32_t kernel_cta = attn_kernel_cta_tile_q(D, group);
+  if (kernel_cta == 0 || kernel_cta != plan->cta_tile_q) return PG_ERR_PLAN_MISMATCH;
+  if (attn_kernel_kv_chunk(D) != plan->kv_chunk) return PG_ERR_PLAN_MISMATCH;
+  if (window_left < -1) return PG_ERR_WINDOW;
+  if (!std::isfinite(sm_scale)) return PG_ERR_NONFINITE;
+  if (plan->num_tokens == 0) return PG_OK;
+  if (!q || !out) return PG_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out)) return PG_ERR_ALIGN;
+  int err = PG_OK;
+  int* st = status_word_existing(&err);
+  if (!st) return err;
+  AttnArgs a;
+  a.plan = plan_dev(plan);
+  a.pool = pool_dev(pool, layer);
+  a.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.ws_o = nullptr;
+  a.ws_ml = nullptr;
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.window_left = window_left;
+  a.num_qo_heads = plan->num_qo_heads;
+  a.group = group;
+  a.cta_tile_q = plan->cta_tile_q;
+  a.kv_chunk = plan->kv_chunk;
+  a.max_chunks = plan->max_chunks;
+  a.status = st;
+  return launch_attn_decode_static(a, D, s) == cudaSuccess ? PG_OK : PG_ERR_CUDA;
 }
 
 int pg_device_status(pg_stream_t stream) {

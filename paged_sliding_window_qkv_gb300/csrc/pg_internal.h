@@ -82,4 +82,8 @@ int32_t attn_kernel_kv_chunk(int32_t head_dim);
 cudaError_t launch_attn_prefill(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);
 cudaError_t launch_attn_decode(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);
 
+// Decode attention with its partials in the library's static scratch (no allocation).
+// The caller has already checked the plan's workspace size against that scratch.
+cudaError_t launch_attn_decode_static(AttnArgs a, int32_t head_dim, cudaStream_t stream);
+
 }  // namespace pg

@@ -94,6 +94,9 @@ _attn256 = _sig("pg_attn_paged_prefill", C.c_int, _P, C.POINTER(pg_pool_t), _I32
                 _I32, _F32, _P, _SZ, _P)
 _attn512 = _sig("pg_attn_paged_prefill_hd512", C.c_int, _P, C.POINTER(pg_pool_t), _I32, _P, _P,
                 _I32, _F32, _P, _SZ, _P)
+_attn_noalloc = _sig("pg_attn_paged_decode_noalloc", C.c_int, _P, C.POINTER(pg_pool_t), _I32,
+                    _P, _P, _I32, _F32, _P)
+PG_NOALLOC_SCRATCH_BYTES = 32 << 20
 _devstat = _sig("pg_device_status", C.c_int, _P)
 _launches = _sig("pg_launch_count", _I64)
 _sstr = _sig("pg_status_string", C.c_char_p, C.c_int)
@@ -238,6 +241,13 @@ def pg_attn_paged_prefill_hd512(plan, pool: pg_pool_t, layer, q, out, window_lef
     return _attn512(plan.handle if plan is not None else None, C.byref(pool), int(layer), _ptr(q),
                     _ptr(out), int(window_left), float(sm_scale), _ptr(workspace), int(ws_bytes),
                     _stream(stream))
+
+
+def pg_attn_paged_decode_noalloc(plan, pool: pg_pool_t, layer, q, out, window_left, sm_scale,
+                                 stream=None) -> int:
+    """Decode attention with the library's static scratch; allocates nothing."""
+    return _attn_noalloc(plan.handle if plan is not None else None, C.byref(pool), int(layer),
+                         _ptr(q), _ptr(out), int(window_left), float(sm_scale), _stream(stream))
 
 
 EXPORTED = ["pg_plan_paged_prefill", "pg_plan_destroy", "pg_plan_info", "pg_rope_table",
