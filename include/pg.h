@@ -58,7 +58,8 @@ enum {
   PG_ERR_STREAM = -15,        /* call stream differs from the plan's stream ([P3] review)      */
   PG_ERR_CUDA = -16,          /* a CUDA runtime call failed                                    */
   PG_ERR_DEVICE_BOUNDS = -17, /* a kernel saw out-of-range metadata and skipped the access     */
-  PG_ERR_ALIGN = -18          /* a device pointer or token stride breaks 16-byte alignment     */
+  PG_ERR_ALIGN = -18,         /* a device pointer or token stride breaks 16-byte alignment     */
+  PG_ERR_DEVICE_TIMEOUT = -19 /* a kernel's bounded wait ran out; its outputs are not valid    */
 };
 
 /* ---------------------------------------------------------------- pool descriptor */
@@ -261,7 +262,7 @@ int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, in
 /* ---------------------------------------------------------------- diagnostics */
 /* Synchronise `stream`, then read and clear the current device's status word.
  * Returns PG_OK, PG_ERR_DEVICE_BOUNDS (a kernel skipped an out-of-range access),
- * or PG_ERR_CUDA. */
+ * PG_ERR_DEVICE_TIMEOUT (a kernel gave up a bounded wait), or PG_ERR_CUDA. */
 int pg_device_status(pg_stream_t stream);
 
 /* Kernels this library has launched since it was loaded (all devices). */

@@ -428,9 +428,11 @@ cudaError_t launch_split(const AttnArgs& a, dim3 grid, cudaStream_t stream) {
 
 }  // namespace
 
-int32_t attn_kernel_cta_tile_q(int32_t head_dim, int32_t group) {
+int32_t attn_kernel_cta_tile_q(int32_t head_dim, int32_t group, int32_t page_size) {
+  if (group <= 0 || group > Dec256::BM) return 0;
+  if (attn_tc_supported(head_dim, group, page_size)) return attn_tc_rows() / group;
   const int32_t rows = head_dim == 256 ? Pre256::BM : head_dim == 512 ? Pre512::BM : 0;
-  if (group <= 0 || rows == 0 || rows % group != 0 || group > Dec256::BM) return 0;
+  if (rows == 0 || rows % group != 0) return 0;
   return rows / group;
 }
 
@@ -438,6 +440,8 @@ int32_t attn_kernel_kv_chunk(int32_t head_dim) { return head_dim == 512 ? 512 : 
 
 cudaError_t launch_attn_prefill(const AttnArgs& a, int32_t head_dim, cudaStream_t stream) {
   if (a.plan.num_work == 0) return cudaSuccess;
+  if (attn_tc_supported(head_dim, a.group, a.pool.page_size))
+    return launch_attn_prefill_tc(a, head_dim, stream);
   dim3 grid(a.plan.num_work, a.pool.num_kv_heads, 1);
   return head_dim == 256 ? launch_split<Pre256>(a, grid, stream)
                          : launch_split<Pre512>(a, grid, stream);

@@ -45,10 +45,14 @@ static bool mul_i64(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_
 static bool add_i64(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
 static bool fits_i32(int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; }
 
-// Query tokens per prefill CTA as the plan derives it (must agree with the kernel's).
-static int32_t plan_cta_tile_q(int32_t head_dim, int32_t group) {
-  if (group <= 0) return 0;
-  const int32_t rows = head_dim == 256 ? 64 : head_dim == 512 ? 32 : 0;
+// Query tokens per prefill CTA as the plan derives it (must agree with the kernel's):
+// 128 rows on the tensor-memory path (head_dim 256/512, group dividing 128, power-of-two page
+// size >= 8), else 64 (head_dim 256) or 32 (head_dim 512) rows on the mma.sync path.
+static int32_t plan_cta_tile_q(int32_t head_dim, int32_t group, int32_t page_size) {
+  if (group <= 0 || group > 16) return 0;
+  const bool tc = (head_dim == 256 || head_dim == 512) && 128 % group == 0 && page_size >= 8 &&
+                  (page_size & (page_size - 1)) == 0;
+  const int32_t rows = tc ? 128 : head_dim == 256 ? 64 : head_dim == 512 ? 32 : 0;
   if (rows == 0 || rows % group != 0) return 0;
   return rows / group;
 }
@@ -130,7 +134,7 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   }
 
   // Tiling derived from the geometry; attention re-derives it from the kernel itself.
-  const int32_t cta = plan_cta_tile_q(D, group);
+  const int32_t cta = plan_cta_tile_q(D, group, ps);
   const int32_t chunk = plan_kv_chunk(D);
   int64_t nwork = 0;
   std::vector<int32_t> wreq, wtok;
@@ -328,11 +332,14 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
   int rc = check_plan_pool(plan, pool, layer, D);
   if (rc) return rc;
   const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
-  const int32_t kernel_cta = attn_kernel_cta_tile_q(D, group);
+  const int32_t kernel_cta = attn_kernel_cta_tile_q(D, group, plan->page_size);
   if (kernel_cta == 0 || kernel_cta != plan->cta_tile_q) return PG_ERR_PLAN_MISMATCH;
   if (attn_kernel_kv_chunk(D) != plan->kv_chunk) return PG_ERR_PLAN_MISMATCH;
   if (window_left < -1) return PG_ERR_WINDOW;
   if (!std::isfinite(sm_scale)) return PG_ERR_NONFINITE;
+  if (!plan->decode && attn_tc_supported(D, group, plan->page_size) &&
+      (int64_t)pool->num_pages * 2 * pool->num_kv_heads * pool->page_size > INT32_MAX)
+    return PG_ERR_I32_OVERFLOW;  // tensor-map row coordinates are int32
   if (plan->num_tokens == 0) return PG_OK;
   if (!q || !out) return PG_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return PG_ERR_ALIGN;
@@ -503,7 +510,7 @@ int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, in
   int rc = check_plan_pool(plan, pool, layer, D);
   if (rc) return rc;
   const int32_t group = plan->num_qo_heads / plan->num_kv_heads;
-  const int32_t kernel_cta = attn_kernel_cta_tile_q(D, group);
+  const int32_t kernel_cta = attn_kernel_cta_tile_q(D, group, plan->page_size);
   if (kernel_cta == 0 || kernel_cta != plan->cta_tile_q) return PG_ERR_PLAN_MISMATCH;
   if (attn_kernel_kv_chunk(D) != plan->kv_chunk) return PG_ERR_PLAN_MISMATCH;
   if (window_left < -1) return PG_ERR_WINDOW;
@@ -542,6 +549,7 @@ int pg_device_status(pg_stream_t stream) {
     return PG_ERR_CUDA;
   if (cudaMemsetAsync(st, 0, sizeof(int), s) != cudaSuccess) return PG_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return PG_ERR_CUDA;
+  if (h & kStatusTimeout) return PG_ERR_DEVICE_TIMEOUT;
   return h ? PG_ERR_DEVICE_BOUNDS : PG_OK;
 }
 
@@ -568,6 +576,7 @@ const char* pg_status_string(int s) {
     case PG_ERR_CUDA: return "CUDA runtime error";
     case PG_ERR_DEVICE_BOUNDS: return "a kernel skipped an out-of-range access";
     case PG_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case PG_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait and returned early";
     default: return "unknown status";
   }
 }

@@ -64,6 +64,8 @@ struct AttnArgs {
 
 // Device status word: set by kernels that skip an out-of-range access.
 constexpr int kStatusBounds = 1;
+// Device status word: a bounded wait inside a kernel ran out of time.
+constexpr int kStatusTimeout = 2;
 
 // Launch counter shared by all launchers.
 void count_launch();
@@ -76,7 +78,11 @@ cudaError_t launch_prep_hd512(const PrepArgs& a, cudaStream_t stream);
 
 // Query tokens per CTA of the prefill attention kernel for this geometry, or 0 when the
 // kernel does not support it. Defined next to the kernels (the kernel's own derivation).
-int32_t attn_kernel_cta_tile_q(int32_t head_dim, int32_t group);
+int32_t attn_kernel_cta_tile_q(int32_t head_dim, int32_t group, int32_t page_size);
+// tcgen05 prefill kernel: geometry it handles, rows per CTA, launch.
+bool attn_tc_supported(int32_t head_dim, int32_t group, int32_t page_size);
+int32_t attn_tc_rows();
+cudaError_t launch_attn_prefill_tc(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);
 // Keys per split-KV chunk of the decode kernel.
 int32_t attn_kernel_kv_chunk(int32_t head_dim);
 cudaError_t launch_attn_prefill(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);

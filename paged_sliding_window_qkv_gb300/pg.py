@@ -44,6 +44,7 @@ PG_ERR_STREAM = -15
 PG_ERR_CUDA = -16
 PG_ERR_DEVICE_BOUNDS = -17
 PG_ERR_ALIGN = -18
+PG_ERR_DEVICE_TIMEOUT = -19
 
 
 class PgError(RuntimeError):
