@@ -293,9 +293,11 @@ attn_split_kernel(AttnArgs a) {
       __nv_bfloat16* P = sP + sm_row * C::PLD + sm_sub * C::VPT;
 #pragma unroll
       for (int v = 0; v < C::VPT; v += 2) {
-        const float p0 = exp2f(s[v] - m_use), p1 = exp2f(s[v + 1] - m_use);
-        sum += p0 + p1;
-        *reinterpret_cast<__nv_bfloat162*>(P + v) = __floats2bfloat162_rn(p0, p1);
+        // sum the bf16-rounded weights that the PV product uses (O / l stays an exact
+        // weighted average of V rows)
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(exp2f(s[v] - m_use), exp2f(s[v + 1] - m_use));
+        sum += __bfloat162float(pb.x) + __bfloat162float(pb.y);
+        *reinterpret_cast<__nv_bfloat162*>(P + v) = pb;
       }
 #pragma unroll
       for (int off = C::TPR / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);

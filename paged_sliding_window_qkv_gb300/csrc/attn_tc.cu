@@ -9,18 +9,24 @@
 // in shared memory) and walks the 64-key tiles of its visible key range, skipping
 // tiles outside the causal window.
 //
-//   warp 0      producer: TMA loads of Q (once) and of K/V page rows into a ring of
-//               32 KB slots, one box per (page, 64-wide d chunk), 128B-swizzled;
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (M=128, N=64, K=16 steps,
-//               both operands from shared memory), then O += P V with P read from TMEM
-//               (M=128, N=256, K=16 steps); completion is signalled with tcgen05.commit;
-//   warps 2..5  softmax: one thread per query row, S row read from TMEM, masked, online
+//   warps 0, 10..12 producers (TMA): Q once; K (warps 0, 10) as 2-D boxes of page rows x
+//               64 d (chunk-major); V (warps 11, 12) as one 3-D box per page (page-major);
+//               separate K and V rings of 32 KB slots, 128B-swizzled;
+//   warps 1, 13 MMA issuers (one thread each): S = Q K^T into TMEM (M=128, N=64, K=16
+//               steps; warp 1) and O += P V with P read from TMEM (M=128, N=256, K=16
+//               steps; warp 13); completion is signalled with tcgen05.commit;
+//   warps 2..9  softmax: two threads per query row (each reads the whole S row for the
+//               maximum, exponentiates half of the tile's keys and owns half of O's
+//               columns), S read from TMEM, masked on boundary tiles only, online
 //               softmax in log2 units with lazy rescaling (O is rescaled in TMEM only
-//               when a row maximum grows by more than 2^8), P written back to TMEM as
-//               bf16; then the epilogue normalises O and stores bf16 rows.
+//               when a row maximum outgrows a 2^64 headroom by more than 2^48: bf16 P and
+//               fp32 O and row sums hold the range, and O / l is unchanged), P written back
+//               to TMEM as bf16;
+//               then the epilogue normalises O and stores bf16 rows.
 //
-// TMEM (512 columns): O [0,256) fp32, S double buffer [256,384), P double buffer
-// [384,448). O holds 256 output columns: for head_dim 512 each query tile runs as two
+// TMEM (512 columns): O [0,256) fp32, S double buffer [256,384), P triple buffer
+// [384,480), per-row exchange between the two softmax warps of a lane quarter [480,488).
+// O holds 256 output columns: for head_dim 512 each query tile runs as two
 // CTAs (grid z), each computing the full 512-wide S and half of O.
 //
 // Every wait is bounded (two seconds of %globaltimer); a wait that runs out sets the
@@ -40,23 +46,47 @@ constexpr int kM = 128;            // query rows per CTA
 constexpr int kBN = 64;            // keys per KV tile
 constexpr int kDV = 256;           // output columns per CTA
 constexpr int kSlotBytes = kBN * 256 * 2;  // 64 keys x 256 d bf16 = 32 KB
-constexpr int kThreadsTc = 192;
-constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 384;
+constexpr int kThreadsTc = 448;  // producers 0,10..12; QK issuer 1; PV issuer 13; softmax 2..9
+// Lazy rescaling: a row's reference maximum is set 2^64 above the first maximum it sees and
+// O is rescaled only when a later maximum exceeds the reference by more than 2^48. P stays
+// within [2^-64, 2^48] of the row's true maximum weight: inside bf16's and fp32's range, with
+// the same relative precision, and O / l does not depend on the reference.
+constexpr float kRescaleLog2 = 48.f;
+constexpr float kHeadroomLog2 = 64.f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Two layouts, chosen by the contraction width:
+//  head_dim 256 (QT): Q lives in TMEM (QK reads A from TMEM like PV does), which frees shared
+//    memory for 7 ring slots (K 3 tiles, V 4 tiles). TMEM: O [0,256), Q [256,384),
+//    S [384,448) (one buffer), P [448,512) (two buffers). MMA order QK(j), PV(j-1), QK(j+1):
+//    the single S buffer is released as soon as the softmax has read it.
+//  head_dim 512: Q (128 KB) stays in shared memory; 3 ring slots (K 2 x 256 d, V 1).
+//    TMEM: O [0,256), S [256,384) (two buffers), P [384,480) (three buffers).
+//    MMA order QK(j), PV(j-2).
 template <int DQK>
 struct TcCfg {
-  static constexpr int PARTS = DQK / 256 + 1;  // K slots + one V slot per tile
-  static constexpr int NS = DQK == 256 ? 5 : 3;
-  static constexpr int Q_BYTES = kM * DQK * 2;
+  static constexpr bool QT = DQK == 256;
+  static constexpr int KP = DQK / 256;          // K slots per tile (256 d each)
+  static constexpr int NKR = QT ? 3 : 1;        // tiles in the K ring
+  static constexpr int NVR = QT ? 4 : 1;        // tiles in the V ring
+  static constexpr int NS = NKR * KP + NVR;
+  static constexpr int Q_BYTES = QT ? 0 : kM * DQK * 2;
   static constexpr int SMEM_DATA = Q_BYTES + NS * kSlotBytes;
-  static constexpr int NBAR = 2 * NS + 11;
-  static constexpr int SMEM = SMEM_DATA + NBAR * 8 + 16 + 1024;  // + barriers, tmem addr, align
+  static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
+  static constexpr int NBAR = 2 * NS + 21;      // ..., 4 per-producer fix-up barriers last
+  static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
+  static constexpr int NSB = QT ? 1 : 2;        // S buffers
+  static constexpr int NPB = QT ? 2 : 3;        // P buffers
+  static constexpr int LAG = QT ? 1 : 2;        // PV(j - LAG) is issued after QK(j)
+  static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = QT ? 384 : 256, TM_P = QT ? 448 : 384;
 };
 
 struct TcArgs {
   PlanDev plan;
+  const __nv_bfloat16* q;
   __nv_bfloat16* out;
+  const __nv_bfloat16* pool_layer;  // pool base of the called layer
+  int64_t stride_page, stride_kv, stride_head;
   int32_t num_qo_heads, group, cta_tile_q, window_left;
   int32_t page_size, num_pages, num_kv_heads, box_rows;
   float scale_log2;
@@ -192,6 +222,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       PG_W8(0), PG_W8(8), PG_W8(16), PG_W8(24)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      PG_W8(0), PG_W8(8)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -214,6 +251,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// 2^x with the hardware exponential (ex2.approx; -inf gives 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -223,22 +267,30 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 template <int DQK>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-               TcArgs a) {
+               const __grid_constant__ CUtensorMap tm_v, TcArgs a) {
   using C = TcCfg<DQK>;
-  constexpr int PARTS = C::PARTS, NS = C::NS;
+  constexpr int KP = C::KP, NKR = C::NKR, NVR = C::NVR, NS = C::NS;
+  constexpr int NSB = C::NSB, NPB = C::NPB, LAG = C::LAG;
+  constexpr uint32_t kTmO = C::TM_O, kTmQ = C::TM_Q, kTmS = C::TM_S, kTmP = C::TM_P;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sSlots = base + C::Q_BYTES;
-  const uint32_t bars = base + C::SMEM_DATA;
+  float* xl = reinterpret_cast<float*>(gbase + C::SMEM_DATA);  // [2 halves][128 rows]
+  const uint32_t bars = base + C::SMEM_DATA + C::XL_BYTES;
   auto FULL = [&](int s) { return bars + 8u * s; };
   auto EMPTY = [&](int s) { return bars + 8u * (NS + s); };
   const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
-                 PVDONE = SFULL + 48, QFULL = SFULL + 64, FIXB = SFULL + 72,
-                 DRAIN = SFULL + 80;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::SMEM_DATA + C::NBAR * 8);
+                 PVDONE = SFULL + 56, QFULL = SFULL + 80, FIXB = SFULL + 88,
+                 DRAIN = SFULL + 96, PAIRB = SFULL + 104,  // PAIRB: 4 barriers, one per lane quarter
+                 FIXV = SFULL + 136;
+  // ring slots: K slots of tile j, then V slot of tile j
+  auto KSLOT = [&](int32_t j, int pp) { return (int)(j % NKR) * KP + pp; };
+  auto VSLOT = [&](int32_t j) { return NKR * KP + (int)(j % NVR); };
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(gbase + C::SMEM_DATA + C::XL_BYTES + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -268,18 +320,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(FULL(s), 1);
+      mbar_init(FULL(s), 2);
       mbar_init(EMPTY(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SFULL + 8 * b, 1);
-      mbar_init(SFREE + 8 * b, 4);
-      mbar_init(PFULL + 8 * b, 4);
+      mbar_init(SFREE + 8 * b, 8);
+    }
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(PFULL + 8 * b, 8);
       mbar_init(PVDONE + 8 * b, 1);
     }
-    mbar_init(QFULL, 1);
+    mbar_init(QFULL, C::QT ? 8 : 1);  // QT: the eight softmax warps store Q into TMEM
     mbar_init(FIXB, 1);
-    mbar_init(DRAIN, 1);
+    mbar_init(FIXV, 1);
+    for (int f = 0; f < 4; ++f) mbar_init(bars + 8u * (C::NBAR - 4 + f), 1);
+    mbar_init(DRAIN, 2);  // one final commit from each MMA-issuing thread
+    for (int q = 0; q < 4; ++q) mbar_init(PAIRB + 8 * q, 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -292,161 +349,231 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    int issued = 0;
+  if (warp == 0 || (warp >= 10 && warp <= 12)) {
+    // ------------------------------------------------------------ producers
+    // TMA throughput here is bounded by how fast one warp can issue copies, so four warps
+    // issue them: warps 0 and 10 load K (2-D boxes of BR rows x 64 d, one per lane, in the
+    // chunk-major 128B-swizzled layout QK's B operand needs), warps 11 and 12 load V (one
+    // 3-D box per page: BR rows x 256 d, landing page-major, which PV's MN-major B operand
+    // reads with a chunk stride of BR*128 bytes). Warp 0 also loads Q once.
+    const bool is_v = warp >= 11;
+    const int pw = (warp == 0 || warp == 11) ? 0 : 1;   // which half of the tile's boxes
+    const uint32_t FIX = bars + 8u * (C::NBAR - 4 + (warp == 0 ? 0 : warp - 9));
     uint32_t fix_phase = 0;
     bool ok = true;
-    if (lane == 0) {
+    if (!C::QT && lane == 0 && warp == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
       mbar_expect_tx(QFULL, C::Q_BYTES);
       for (int c = 0; c < DQK / 64; ++c)
         tma_load_3d(sQ + c * (kM * 128), &tm_q, c * 64, g * G, q0 + tok0, QFULL);
     }
-    const int BR = a.box_rows;          // rows per TMA box: min(page_size, 64)
-    const int nbox = kBN / BR;          // boxes per 64-key tile per d chunk
+    if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(is_v ? &tm_v : &tm_kv) : "memory");
+    const int BR = a.box_rows;          // key rows per box: min(page_size, 64)
+    const int nbox = kBN / BR;          // boxes (pages or page parts) per 64-key tile
     const int64_t head_rows = (int64_t)ps;
-    for (int32_t j = 0; j < ntiles && ok; ++j) {
-      const int32_t kb = kb0 + j * kBN;
-      // page rows of this tile, checked against the pool (second layer of defence)
-      int32_t row_k = -1;   // lane b < nbox: tensor row of box b's first K row, or -1
-      bool bad = false;
-      if (lane < nbox) {
-        const int32_t ks = kb + lane * BR;
-        if (ks < kv_len) {
-          const int32_t pidx = kvp0 + ks / ps;
-          const int32_t page = (pidx < kvp1 && pidx < pl.num_page_ids) ? pl.page_ids[pidx] : -1;
-          if (page < 0 || page >= a.num_pages) {
-            bad = true;
-          } else {
-            row_k = (int32_t)((((int64_t)page * 2) * a.num_kv_heads + g) * head_rows + (ks % ps));
-          }
-        }
-      }
+    // this warp's boxes: b = pw, pw + 2, ... (< nbox); K: one lane per (box, d chunk)
+    // lane -> (box, chunk): K lanes 4*i + c take box pw + 2*i, chunk c; V lanes i take box pw + 2*i
+    const int my_box = is_v ? pw + 2 * lane : pw + 2 * (lane >> 2);
+    const int my_chunk = is_v ? 0 : (lane & 3);
+    const bool box_lane = my_box < nbox && (is_v ? lane < 32 : true);
+    auto page_of = [&](int32_t t) -> int32_t {  // raw page id of this lane's box (-1: past kv_len)
+      if (!box_lane) return -1;
+      const int32_t ks = kb0 + t * kBN + my_box * BR;
+      if (ks >= kv_len) return -1;
+      const int32_t pidx = kvp0 + ks / ps;
+      return (pidx < kvp1 && pidx < pl.num_page_ids) ? pl.page_ids[pidx] : a.num_pages;
+    };
+    auto issue_part = [&](int s, int round, int d0, int32_t t, int32_t page) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(EMPTY(s), (round & 1) ^ 1, abort_flag, a.status)))
+        return false;
+      const int32_t kb = kb0 + t * kBN;
+      const bool past = !box_lane || kb + my_box * BR >= kv_len;
+      const bool bad = !past && (page < 0 || page >= a.num_pages);
       const bool any_bad = __any_sync(0xffffffffu, bad);
       if (any_bad && lane == 0) atomicOr(a.status, kStatusBounds);
-      const bool fix = any_bad || (kb + kBN > kv_len);
-      for (int pp = 0; pp < PARTS; ++pp) {
-        const int part = j * PARTS + pp;
-        const int s = part % NS;
-        if (!__all_sync(0xffffffffu, mbar_wait(EMPTY(s), ((part / NS) & 1) ^ 1, abort_flag, a.status))) {
-          ok = false;
-          break;
-        }
-        const bool is_v = pp == PARTS - 1;
-        const int d0 = is_v ? dh * 256 : pp * 256;
-        // V rows sit Hkv head-blocks after the K rows of the same page
-        const int32_t vshift = is_v ? (int32_t)(a.num_kv_heads * head_rows) : 0;
-        int nloaded = __popc(__ballot_sync(0xffffffffu, lane < nbox && row_k >= 0));
-        const uint32_t bytes = (uint32_t)nloaded * 4u * BR * 128u;
-        const uint32_t slot = sSlots + s * kSlotBytes;
-        const uint32_t bar = fix ? FIXB : FULL(s);
-        if (lane == 0 && bytes > 0) mbar_expect_tx(bar, bytes);
-        __syncwarp();
-        if (lane < nbox && row_k >= 0) {
-          for (int c = 0; c < 4; ++c)
-            tma_load_2d(slot + c * (kBN * 128) + lane * BR * 128, &tm_kv, d0 + c * 64,
-                        row_k + vshift, bar);
-        }
-        ++issued;
-        if (fix) {
-          if (bytes > 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(FIXB, fix_phase, abort_flag, a.status))) {
-              ok = false;
-              break;
-            }
-            fix_phase ^= 1u;
-          }
-          // zero the rows of keys the tile must not read: past kv_len or on a bad page
-          for (int k = 0; k < kBN; ++k) {
-            const int b = k / BR;
-            const int32_t rb = __shfl_sync(0xffffffffu, row_k, b);
-            if (kb + k < kv_len && rb >= 0) continue;
-            // 4 chunks x 128 bytes = 32 lanes x 16 bytes
-            const int c = lane >> 3, w16 = lane & 7;
-            uint4* p = reinterpret_cast<uint4*>(gbase + (slot - base) + c * (kBN * 128) + k * 128) + w16;
-            *p = make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(FULL(s));
+      const bool load = !past && !bad;
+      // V rows past kv_len (partial last page) must read as zeros; K rows there are masked
+      const bool fix = any_bad || (is_v && __any_sync(0xffffffffu, box_lane && kb + my_box * BR + BR > kv_len));
+      const uint32_t box_bytes = is_v ? (uint32_t)BR * 512u : (uint32_t)BR * 128u;
+      const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, load)) * box_bytes;
+      const uint32_t slot = sSlots + s * kSlotBytes;
+      const uint32_t bar = fix ? FIX : FULL(s);
+      if (lane == 0) {
+        if (bytes > 0) mbar_expect_tx(bar, bytes);
+        else if (!fix) mbar_arrive(bar);
+      }
+      __syncwarp();
+      if (load) {
+        const int32_t row = (int32_t)((((int64_t)page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + g) *
+                                          head_rows + ((kb + my_box * BR) % ps));
+        if (is_v) {
+          tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
+        } else {
+          tma_load_2d(slot + my_chunk * (kBN * 128) + my_box * (BR * 128), &tm_kv, d0 + my_chunk * 64,
+                      row, bar);
         }
       }
+      if (fix) {
+        if (bytes > 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(FIX, fix_phase, abort_flag, a.status))) return false;
+          fix_phase ^= 1u;
+        }
+        // zero this warp's rows that must not be read: keys past kv_len, keys on bad pages
+        for (int b = pw; b < nbox; b += 2) {
+          const int32_t pb = __shfl_sync(0xffffffffu, page, is_v ? (b - pw) / 2 : 4 * ((b - pw) / 2));
+          for (int r = 0; r < BR; ++r) {
+            const int32_t key = kb + b * BR + r;
+            if (key < kv_len && pb >= 0 && pb < a.num_pages) continue;
+            const int c = lane >> 3, w16 = lane & 7;  // 4 chunks x 128 bytes = 32 lanes x 16 bytes
+            const uint32_t off = is_v ? b * (BR * 512) + c * (BR * 128) + r * 128
+                                      : c * (kBN * 128) + (b * BR + r) * 128;
+            *(reinterpret_cast<uint4*>(gbase + (slot - base) + off) + w16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(FULL(s));
+      }
+      return true;
+    };
+    int32_t qa = ntiles > 0 ? page_of(0) : -1;
+    int32_t qb = ntiles > 1 ? page_of(1) : -1;
+    for (int32_t t = 0; ok && t < ntiles; ++t) {
+      const int32_t qc = t + 2 < ntiles ? page_of(t + 2) : -1;  // read two tiles ahead
+      if (!is_v) {
+        for (int pp = 0; ok && pp < KP; ++pp)
+          ok = issue_part(KSLOT(t, pp), (int)(t / NKR), pp * 256, t, qa);
+      } else {
+        ok = issue_part(VSLOT(t), (int)(t / NVR), dh * 256, t, qa);
+      }
+      qa = qb;
+      qb = qc;
     }
     if (!ok) {
-      // drain: let every load this warp issued land before the CTA frees its memory
-      for (int p = max(0, issued - NS); p < issued; ++p) {
-        const int s = p % NS;
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(FULL(s), (p / NS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
-        }
+      // aborting: give the copies this warp already issued time to land (they complete within
+      // microseconds) before the CTA releases its shared memory
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 100000ull) {
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 13) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread can issue a tcgen05.mma only every ~120-180 cycles, less than one
+    // M128 x N64 x K16 instruction takes on the tensor pipe, so QK (warp 1) and PV (warp 13)
+    // are issued from two threads; they accumulate into disjoint TMEM (S and O) and are
+    // ordered against each other only through the barriers.
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16(kM, kBN, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(kM, kDV, true);
-      bool ok = mbar_wait(QFULL, 0, abort_flag, a.status);
-      for (int32_t j = 0; ok && j <= ntiles; ++j) {
-        if (j < ntiles) {
-          const int b = j & 1, u = j >> 1;
-          ok = mbar_wait(SFREE + 8 * b, (u & 1) ^ 1, abort_flag, a.status);
-          uint32_t kslot[PARTS - 1];
-          for (int pp = 0; ok && pp < PARTS - 1; ++pp) {
-            const int part = j * PARTS + pp;
-            kslot[pp] = sSlots + (part % NS) * kSlotBytes;
-            ok = mbar_wait(FULL(part % NS), (part / NS) & 1, abort_flag, a.status);
+      bool ok = true;
+      if (warp == 1) {
+        ok = mbar_wait(QFULL, 0, abort_flag, a.status);
+        for (int32_t j = 0; ok && j < ntiles; ++j) {
+          const int sb = j % NSB;
+          ok = mbar_wait(SFREE + 8 * sb, ((j / NSB) & 1) ^ 1, abort_flag, a.status);
+          uint32_t kslot[KP];
+          for (int pp = 0; ok && pp < KP; ++pp) {
+            const int sidx = KSLOT(j, pp);
+            kslot[pp] = sSlots + sidx * kSlotBytes;
+            ok = mbar_wait(FULL(sidx), (j / NKR) & 1, abort_flag, a.status);
           }
           if (!ok) break;
           tc_fence_after();
-          const uint32_t dS = tmem + kTmS + b * kBN;
-#pragma unroll 4
-          for (int kk = 0; kk < DQK / 16; ++kk) {
-            const uint32_t qa = sQ + (kk >> 2) * (kM * 128) + (kk & 3) * 32;
-            const int kin = kk & 15;
-            const uint32_t ka = kslot[kk >> 4] + (kin >> 2) * (kBN * 128) + (kin & 3) * 32;
-            mma_ss(dS, sdesc(qa, 16, 1024), sdesc(ka, 16, 1024), IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint32_t dS = tmem + kTmS + sb * kBN;
+          // descriptors advance by 32 B per K step inside a 128-byte swizzle row and by one
+          // 64-column chunk (kBN or kM rows x 128 B) every 4 steps
+          const uint64_t kd0 = sdesc(kslot[0], 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4);
+            if constexpr (C::QT) {
+              mma_ts(dS, tmem + kTmQ + kk * 8, kd, IDESC_QK, kk > 0 ? 1u : 0u);
+            } else {
+              const uint64_t qd = sdesc(sQ, 16, 1024) + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+              mma_ss(dS, qd, kd, IDESC_QK, kk > 0 ? 1u : 0u);
+            }
           }
-          mma_commit(SFULL + 8 * b);
-          for (int pp = 0; pp < PARTS - 1; ++pp) mma_commit(EMPTY((j * PARTS + pp) % NS));
+          if constexpr (KP > 1) {
+            const uint64_t kd1 = sdesc(kslot[KP - 1], 16, 1024);
+#pragma unroll
+            for (int kk = 16; kk < 32; ++kk) {
+              const int kin = kk & 15;
+              const uint64_t kd = kd1 + (uint64_t)(((kin >> 2) * (kBN * 128) + (kin & 3) * 32) >> 4);
+              const uint64_t qd = sdesc(sQ, 16, 1024) + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+              mma_ss(dS, qd, kd, IDESC_QK, 1u);
+            }
+          }
+          mma_commit(SFULL + 8 * sb);
+          for (int pp = 0; pp < KP; ++pp) mma_commit(EMPTY(KSLOT(j, pp)));
         }
-        if (j >= 1) {
-          const int32_t jp = j - 1;
-          const int b = jp & 1, u = jp >> 1;
-          const int part = jp * PARTS + PARTS - 1;
-          const int s = part % NS;
-          ok = mbar_wait(FULL(s), (part / NS) & 1, abort_flag, a.status) &&
-               mbar_wait(PFULL + 8 * b, u & 1, abort_flag, a.status);
+      } else {
+        const int BR = a.box_rows;
+        const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 512u;
+        for (int32_t jp = 0; ok && jp < ntiles; ++jp) {
+          const int pb = jp % NPB;
+          const int sidx = VSLOT(jp);
+          ok = mbar_wait(FULL(sidx), (jp / NVR) & 1, abort_flag, a.status) &&
+               mbar_wait(PFULL + 8 * pb, (jp / NPB) & 1, abort_flag, a.status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t vs = sSlots + s * kSlotBytes;
+          const uint32_t vs = sSlots + sidx * kSlotBytes;
+          // V slot: page-major boxes of BR rows, each [4 chunks][BR rows][128 B]
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
-            mma_ts(tmem + kTmO, tmem + kTmP + b * (kBN / 2) + kk * 8,
-                   sdesc(vs + kk * 2048, kBN * 128, 1024), IDESC_PV, (jp > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t key = 16u * kk;
+            const uint32_t va = vs + (key / BR) * (BR * 512u) + (key % BR) * 128u;
+            mma_ts(tmem + kTmO, tmem + kTmP + pb * (kBN / 2) + kk * 8, sdesc(va, lbo, sbo), IDESC_PV,
+                   (jp > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(EMPTY(s));
-          mma_commit(PVDONE + 8 * b);
+          mma_commit(EMPTY(sidx));
+          mma_commit(PVDONE + 8 * pb);
         }
       }
       // arrives once every MMA this thread issued has completed; waited on before TMEM is freed
       mma_commit(DRAIN);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 9) {
     // ------------------------------------------------------------ softmax + epilogue
+    // Two warps per TMEM lane quarter: half h = 0 owns key columns [0,32) of each tile and
+    // output columns [0,128), half h = 1 the other halves. The row maximum of a tile is
+    // shared through shared memory; each half keeps its own partial row sum.
     const int quarter = warp & 3;
+    const int h = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const bool rvalid = row < ntok * G;
     const int32_t prow = sp + tok0 + row / G;
     const int32_t rlo = W >= 0 ? max(0, prow - W) : 0;
     const int32_t rhi = min(prow + 1, kv_len);
+    const uint32_t pair_bar = PAIRB + 8 * quarter;  // meeting point of the two warps sharing these rows
+    uint32_t pair_phase = 0;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    constexpr int HC = kBN / 2;  // key columns per half
+    if constexpr (C::QT) {
+      // Q rows into TMEM: this thread stores its row's d columns [128h, 128h + 128) as bf16
+      // pairs (64 TMEM columns), the A operand layout of QK
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + ((int64_t)(q0 + tok0 + row / G) * Hq + g * G + row % G) * DQK + h * 128);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = rvalid ? __ldg(src + half * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+        tmem_st32(tl + kTmQ + h * 64 + half * 32, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(QFULL);
+    }
     for (int32_t j = 0; ok && j < ntiles; ++j) {
-      const int b = j & 1, u = j >> 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(SFULL + 8 * b, u & 1, abort_flag, a.status))) { ok = false; break; }
+      const int b = j % NSB;
+      if (!__all_sync(0xffffffffu, mbar_wait(SFULL + 8 * b, (j / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
       tc_fence_after();
+      // both warps of the pair read the whole 64-key row: the row maximum needs no exchange
       uint32_t sv[kBN];
       tmem_ld32(tl + kTmS + b * kBN, sv);
       tmem_ld32(tl + kTmS + b * kBN + 32, sv + 32);
@@ -455,67 +582,99 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(SFREE + 8 * b);
       const int32_t kb = kb0 + j * kBN;
-      float s[kBN];
-      float mx = -INFINITY;
+      const bool interior = __all_sync(0xffffffffu, rvalid && kb >= rlo && kb + kBN <= rhi);
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (interior) {
 #pragma unroll
-      for (int k = 0; k < kBN; ++k) {
-        const int32_t key = kb + k;
-        const bool vis = rvalid && key >= rlo && key < rhi;
-        s[k] = vis ? __uint_as_float(sv[k]) * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[k]);
+        for (int k = 0; k < kBN; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < kBN; ++k) {
+          const int32_t key = kb + k;
+          const bool vis = rvalid && key >= rlo && key < rhi;
+          sv[k] = vis ? sv[k] : 0xFF800000u;  // -inf
+          m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
+        }
       }
+      // scores in log2 units; a positive scale keeps the maximum where it was
+      const float raw_mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      float mx;
+      if (a.scale_log2 > 0.f) {
+        mx = raw_mx * a.scale_log2;
+      } else {
+        mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kBN; ++k) mx = fmaxf(mx, __uint_as_float(sv[k]) * a.scale_log2);
+      }
+      float s[HC];
+#pragma unroll
+      for (int k = 0; k < HC; ++k) s[k] = __uint_as_float(h ? sv[HC + k] : sv[k]) * a.scale_log2;
       float alpha = 1.f;
       bool resc = false;
-      if (mx > m_ref + 8.f) {
-        alpha = m_ref == -INFINITY ? 0.f : exp2f(m_ref - mx);
+      if (mx > m_ref + kRescaleLog2) {
+        // new reference with headroom above this maximum, so later growth rarely rescales
+        const float m_new = mx + kHeadroomLog2;
+        alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_new);
         resc = m_ref != -INFINITY;
         l *= alpha;
-        m_ref = mx;
+        m_ref = m_new;
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         const int jp = j - 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp & 1), (jp >> 1) & 1, abort_flag, a.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp % NPB), (jp / NPB) & 1, abort_flag, a.status))) { ok = false; break; }
         tc_fence_after();
-        for (int c = 0; c < kDV / 32; ++c) {
+        for (int c = 0; c < kDV / 64; ++c) {
           uint32_t o[32];
-          tmem_ld32(tl + kTmO + c * 32, o);
+          const uint32_t col = kTmO + h * (kDV / 2) + c * 32;
+          tmem_ld32(tl + col, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tl + kTmO + c * 32, o);
+          tmem_st32(tl + col, o);
         }
         tmem_wait_st();
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      float sum = 0.f;
-      uint32_t pk[kBN / 2];
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[HC / 2];
 #pragma unroll
-      for (int k = 0; k < kBN / 2; ++k) {
-        const float p0 = exp2f(s[2 * k] - mu), p1 = exp2f(s[2 * k + 1] - mu);
-        sum += p0 + p1;
-        pk[k] = pack_bf16(p0, p1);
+      for (int k = 0; k < HC / 2; ++k) {
+        // the row sum adds the bf16-rounded weights the PV product uses, so O / l is an
+        // exact weighted average of V rows (a dominant key's rounding cancels)
+        pk[k] = pack_bf16(ex2(s[2 * k] - mu), ex2(s[2 * k + 1] - mu));
+        sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
       }
-      l += sum;
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * b, ((j >> 1) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      const int pb = j % NPB;
+      if (j >= NPB && !__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * pb, ((j / NPB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
       tc_fence_after();
-      tmem_st32(tl + kTmP + b * (kBN / 2), pk);
+      tmem_st16(tl + kTmP + pb * (kBN / 2) + h * (HC / 2), pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(PFULL + 8 * b);
+      if (lane == 0) mbar_arrive(PFULL + 8 * pb);
     }
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl & 1), (jl >> 1) & 1, abort_flag, a.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NPB), (jl / NPB) & 1, abort_flag, a.status));
+    }
+    // the row sum is the sum of both halves' partial sums
+    if (ok) {
+      // swap partial row sums with the partner warp through shared memory
+      xl[h * kM + row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pair_bar);
+      ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status));
+      if (ok) l = xl[row] + xl[kM + row];
     }
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* dst = a.out + ((int64_t)(q0 + tok0 + row / G) * Hq + g * G + row % G) * DQK +
-                           dh * kDV;
-      for (int c = 0; c < kDV / 32; ++c) {
+                           dh * kDV + h * (kDV / 2);
+      for (int c = 0; c < kDV / 64; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + kTmO + c * 32, o);
+        tmem_ld32(tl + kTmO + h * (kDV / 2) + c * 32, o);
         tmem_wait_ld();
         if (ntiles == 0) {
 #pragma unroll
@@ -576,7 +735,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int32_t G = a.group, TQ = a.cta_tile_q;
-  CUtensorMap tq, tkv;
+  CUtensorMap tq, tkv, tv;
   {
     cuuint64_t dims[3] = {(cuuint64_t)DQK, (cuuint64_t)a.num_qo_heads,
                           (cuuint64_t)a.plan.num_tokens};
@@ -601,8 +760,21 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  {
+    // V: dims (64 d, row, d chunk); one box = br rows x 4 chunks (256 d) of one page
+    const cuuint64_t rows = (cuuint64_t)a.pool.num_pages * 2 * a.pool.num_kv_heads * ps;
+    cuuint64_t dims[3] = {64, rows, (cuuint64_t)DQK / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)DQK * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)br, 4};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.pool.layer_base, dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   TcArgs t;
   t.plan = a.plan;
+  t.q = a.q;
   t.out = a.out;
   t.num_qo_heads = a.num_qo_heads;
   t.group = G;
@@ -612,6 +784,10 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   t.num_pages = a.pool.num_pages;
   t.num_kv_heads = a.pool.num_kv_heads;
   t.box_rows = br;
+  t.pool_layer = a.pool.layer_base;
+  t.stride_page = a.pool.stride_page;
+  t.stride_kv = a.pool.stride_kv;
+  t.stride_head = a.pool.stride_head;
   t.scale_log2 = a.sm_scale_log2;
   t.status = a.status;
 
@@ -627,7 +803,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
     configured[dev] = true;
   }
   dim3 grid(a.plan.num_work, a.pool.num_kv_heads, DQK / kDV);
-  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, t);
+  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, tv, t);
   count_launch();
   return cudaGetLastError();
 }
