@@ -79,6 +79,10 @@ struct TcCfg {
   static constexpr int NPB = QT ? 2 : 3;        // P buffers
   static constexpr int LAG = QT ? 1 : 2;        // PV(j - LAG) is issued after QK(j)
   static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = QT ? 384 : 256, TM_P = QT ? 448 : 384;
+  // CTA pairs (clusters of two) share K/V loads by TMA multicast: head_dim 256 pairs two adjacent
+  // query tiles (sharing K and V over their union key range); head_dim 512 pairs the two
+  // output-column halves of one query tile (sharing K; each loads its own half of V)
+  static constexpr bool SHARE_V = QT;
 };
 
 struct TcArgs {
@@ -122,14 +126,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that lets the hardware suspend the thread until the phase completes (or kSuspendNs
+// pass) instead of spinning on the barrier word.
+constexpr uint32_t kSuspendNs = 200000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait on the phase of the given parity. Returns false when the CTA is aborting
 // (another role gave up) or when this wait itself runs out of time.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       int* status) {
+__device__ __forceinline__ bool mbar_wait_body(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       atomicOr(status, kStatusTimeout);
@@ -137,6 +154,15 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       return false;
     }
   }
+}
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       int* status) {
+  return mbar_wait_body(bar, parity, abort_flag, status);
+}
+// The same wait inlined, for the MMA-issuing warps.
+__device__ __forceinline__ bool mbar_wait_inline(uint32_t bar, uint32_t parity,
+                                                 volatile int* abort_flag, int* status) {
+  return mbar_wait_body(bar, parity, abort_flag, status);
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -162,6 +188,32 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// TMA loads that land at the same shared-memory offset in both CTAs of the cluster pair and
+// complete transactions on the mbarrier at the same offset in each
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                               uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar), "h"((unsigned short)3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                               int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar), "h"((unsigned short)3)
+      : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -180,25 +232,39 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t acc) {
+// The MMA and commit helpers below are executed by the whole issuing warp and act from lane 0
+// only. The instruction descriptor is an immediate. Measured on this kernel: with the
+// descriptor in a register, or with the issuing lane picked by elect.sync, M128 MMAs issued at
+// one per ~220-290 cycles in many tiles; predicated on lane 0 with an immediate descriptor they
+// keep the tensor pipe full (32-48 cycles per M128 x N64 x K16 instruction).
+template <uint32_t IDESC>
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      "{\n .reg .pred e, p;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n setp.ne.b32 p, %3, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(acc), "n"(IDESC)
       : "memory");
 }
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                       uint32_t acc) {
+template <uint32_t IDESC>
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      "{\n .reg .pred e, p;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n setp.ne.b32 p, %3, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(acc), "n"(IDESC)
+      : "memory");
+}
+// arrive on the mbarrier at this offset in both CTAs of the pair once prior MMAs complete
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n}\n" ::"r"(bar), "h"((unsigned short)3)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n .reg .pred e;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
       : "memory");
 }
 
@@ -307,21 +373,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int32_t kv_len = (kvp1 - kvp0 - 1) * ps + pl.last_page_len[r];
   const int32_t sp = pl.start_pos[r];
   const int32_t W = a.window_left;
-  const int32_t p_first = sp + tok0, p_last = sp + tok0 + ntok - 1;
-  const int32_t lo = W >= 0 ? max(0, p_first - W) : 0;
-  const int32_t hi = min(p_last + 1, kv_len);
+  const uint32_t rank = cluster_rank();
+  // key range: this tile's visible keys, widened to the pair's union when the pair shares V
+  int32_t lo, hi;
+  {
+    const int32_t p_first = sp + tok0, p_last = sp + tok0 + ntok - 1;
+    lo = W >= 0 ? max(0, p_first - W) : 0;
+    hi = min(p_last + 1, kv_len);
+    if constexpr (C::SHARE_V) {
+      const int32_t pt0 = pl.work_tok0[item ^ 1];  // partner: same request, adjacent tile
+      const int32_t pn = min(a.cta_tile_q, pl.qo_indptr[r + 1] - q0 - pt0);
+      lo = min(lo, W >= 0 ? max(0, sp + pt0 - W) : 0);
+      hi = max(hi, min(sp + pt0 + pn, kv_len));
+    }
+  }
   const int32_t kb0 = lo & ~(kBN - 1);
   const int32_t ntiles = hi > kb0 ? (hi - kb0 + kBN - 1) / kBN : 0;
 
-  // a CTA that finds an earlier CTA timed out returns at once (uniformly, before TMEM)
-  if (threadIdx.x == 0) *abort_flag = *reinterpret_cast<volatile int*>(a.status) & kStatusTimeout;
-  __syncthreads();
-  if (*abort_flag) return;
-  __syncthreads();
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(FULL(s), 2);
-      mbar_init(EMPTY(s), 1);
+      // a shared slot is free again once both CTAs' MMAs have consumed it
+      mbar_init(EMPTY(s), (s < NKR * KP || C::SHARE_V) ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SFULL + 8 * b, 1);
@@ -346,6 +419,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
+  // the peer's barriers must be initialised before any multicast copy or commit reaches them
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -403,14 +478,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         else if (!fix) mbar_arrive(bar);
       }
       __syncwarp();
-      if (load) {
+      // shared parts: the two CTAs split this warp's boxes and multicast them to both
+      const bool shared = !is_v || C::SHARE_V;
+      if (load && (!shared || (uint32_t)((my_box >> 1) & 1) == rank)) {
         const int32_t row = (int32_t)((((int64_t)page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + g) *
                                           head_rows + ((kb + my_box * BR) % ps));
         if (is_v) {
-          tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
+          if (shared) tma_load_3d_mc(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
+          else tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
         } else {
-          tma_load_2d(slot + my_chunk * (kBN * 128) + my_box * (BR * 128), &tm_kv, d0 + my_chunk * 64,
-                      row, bar);
+          tma_load_2d_mc(slot + my_chunk * (kBN * 128) + my_box * (BR * 128), &tm_kv,
+                         d0 + my_chunk * 64, row, bar);
         }
       }
       if (fix) {
@@ -436,18 +514,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       return true;
     };
-    int32_t qa = ntiles > 0 ? page_of(0) : -1;
-    int32_t qb = ntiles > 1 ? page_of(1) : -1;
+    // page ids are read two tiles ahead of the loads that use them
+    constexpr int kLook = 2;
+    int32_t qid[kLook + 1];
+#pragma unroll
+    for (int i = 0; i <= kLook; ++i) qid[i] = i < ntiles ? page_of(i) : -1;
     for (int32_t t = 0; ok && t < ntiles; ++t) {
-      const int32_t qc = t + 2 < ntiles ? page_of(t + 2) : -1;  // read two tiles ahead
+      const int32_t qn = t + kLook + 1 < ntiles ? page_of(t + kLook + 1) : -1;
       if (!is_v) {
         for (int pp = 0; ok && pp < KP; ++pp)
-          ok = issue_part(KSLOT(t, pp), (int)(t / NKR), pp * 256, t, qa);
+          ok = issue_part(KSLOT(t, pp), (int)(t / NKR), pp * 256, t, qid[0]);
       } else {
-        ok = issue_part(VSLOT(t), (int)(t / NVR), dh * 256, t, qa);
+        ok = issue_part(VSLOT(t), (int)(t / NVR), dh * 256, t, qid[0]);
       }
-      qa = qb;
-      qb = qc;
+#pragma unroll
+      for (int i = 0; i < kLook; ++i) qid[i] = qid[i + 1];
+      qid[kLook] = qn;
     }
     if (!ok) {
       // aborting: give the copies this warp already issued time to land (they complete within
@@ -458,80 +540,85 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
   } else if (warp == 1 || warp == 13) {
     // ------------------------------------------------------------ MMA issuers
-    // One thread can issue a tcgen05.mma only every ~120-180 cycles, less than one
-    // M128 x N64 x K16 instruction takes on the tensor pipe, so QK (warp 1) and PV (warp 13)
-    // are issued from two threads; they accumulate into disjoint TMEM (S and O) and are
-    // ordered against each other only through the barriers.
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16(kM, kBN, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16(kM, kDV, true);
-      bool ok = true;
-      if (warp == 1) {
-        ok = mbar_wait(QFULL, 0, abort_flag, a.status);
-        for (int32_t j = 0; ok && j < ntiles; ++j) {
-          const int sb = j % NSB;
-          ok = mbar_wait(SFREE + 8 * sb, ((j / NSB) & 1) ^ 1, abort_flag, a.status);
-          uint32_t kslot[KP];
-          for (int pp = 0; ok && pp < KP; ++pp) {
-            const int sidx = KSLOT(j, pp);
-            kslot[pp] = sSlots + sidx * kSlotBytes;
-            ok = mbar_wait(FULL(sidx), (j / NKR) & 1, abort_flag, a.status);
-          }
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t dS = tmem + kTmS + sb * kBN;
-          // descriptors advance by 32 B per K step inside a 128-byte swizzle row and by one
-          // 64-column chunk (kBN or kM rows x 128 B) every 4 steps
-          const uint64_t kd0 = sdesc(kslot[0], 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4);
-            if constexpr (C::QT) {
-              mma_ts(dS, tmem + kTmQ + kk * 8, kd, IDESC_QK, kk > 0 ? 1u : 0u);
-            } else {
-              const uint64_t qd = sdesc(sQ, 16, 1024) + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
-              mma_ss(dS, qd, kd, IDESC_QK, kk > 0 ? 1u : 0u);
-            }
-          }
-          if constexpr (KP > 1) {
-            const uint64_t kd1 = sdesc(kslot[KP - 1], 16, 1024);
-#pragma unroll
-            for (int kk = 16; kk < 32; ++kk) {
-              const int kin = kk & 15;
-              const uint64_t kd = kd1 + (uint64_t)(((kin >> 2) * (kBN * 128) + (kin & 3) * 32) >> 4);
-              const uint64_t qd = sdesc(sQ, 16, 1024) + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
-              mma_ss(dS, qd, kd, IDESC_QK, 1u);
-            }
-          }
-          mma_commit(SFULL + 8 * sb);
-          for (int pp = 0; pp < KP; ++pp) mma_commit(EMPTY(KSLOT(j, pp)));
+    // QK (warp 1) and PV (warp 13) are issued by two warps; they accumulate into disjoint
+    // TMEM (S and O) and are ordered against each other only through the barriers. Lane 0
+    // waits on the barriers and issues; the other lanes follow it through the loop.
+    constexpr uint32_t IDESC_QK = idesc_bf16(kM, kBN, false);
+    constexpr uint32_t IDESC_PV = idesc_bf16(kM, kDV, true);
+    auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
+      const bool r = lane == 0 ? mbar_wait_inline(bar, parity, abort_flag, a.status) : false;
+      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    };
+    bool ok = true;
+    if (warp == 1) {
+      ok = wait1(QFULL, 0);
+      for (int32_t j = 0; ok && j < ntiles; ++j) {
+        const int sb = j % NSB;
+        ok = wait1(SFREE + 8 * sb, ((j / NSB) & 1) ^ 1);
+        uint32_t kslot[KP];
+        for (int pp = 0; ok && pp < KP; ++pp) {
+          const int sidx = KSLOT(j, pp);
+          kslot[pp] = sSlots + sidx * kSlotBytes;
+          ok = wait1(FULL(sidx), (j / NKR) & 1);
         }
-      } else {
-        const int BR = a.box_rows;
-        const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 512u;
-        for (int32_t jp = 0; ok && jp < ntiles; ++jp) {
-          const int pb = jp % NPB;
-          const int sidx = VSLOT(jp);
-          ok = mbar_wait(FULL(sidx), (jp / NVR) & 1, abort_flag, a.status) &&
-               mbar_wait(PFULL + 8 * pb, (jp / NPB) & 1, abort_flag, a.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t vs = sSlots + sidx * kSlotBytes;
-          // V slot: page-major boxes of BR rows, each [4 chunks][BR rows][128 B]
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t dS = tmem + kTmS + sb * kBN;
+        // descriptors advance by 32 B per K step inside a 128-byte swizzle row and by one
+        // 64-column chunk (kBN or kM rows x 128 B) every 4 steps
+        const uint64_t kd0 = sdesc(kslot[0], 16, 1024);
+        // an opaque per-tile copy of Q's base descriptor keeps the compiler from hoisting all
+        // 32 derived descriptors out of the loop (64 registers)
+        uint64_t qd0 = sdesc(sQ, 16, 1024);
+        asm volatile("mov.b64 %0, %0;" : "+l"(qd0));
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint32_t key = 16u * kk;
-            const uint32_t va = vs + (key / BR) * (BR * 512u) + (key % BR) * 128u;
-            mma_ts(tmem + kTmO, tmem + kTmP + pb * (kBN / 2) + kk * 8, sdesc(va, lbo, sbo), IDESC_PV,
-                   (jp > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4);
+          if constexpr (C::QT) {
+            mma_ts<IDESC_QK>(dS, tmem + kTmQ + kk * 8, kd, kk > 0 ? 1u : 0u);
+          } else {
+            const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+            mma_ss<IDESC_QK>(dS, qd, kd, kk > 0 ? 1u : 0u);
           }
-          mma_commit(EMPTY(sidx));
-          mma_commit(PVDONE + 8 * pb);
         }
+        if constexpr (KP > 1) {
+          const uint64_t kd1 = sdesc(kslot[KP - 1], 16, 1024);
+#pragma unroll
+          for (int kk = 16; kk < 32; ++kk) {
+            const int kin = kk & 15;
+            const uint64_t kd = kd1 + (uint64_t)(((kin >> 2) * (kBN * 128) + (kin & 3) * 32) >> 4);
+            const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+            mma_ss<IDESC_QK>(dS, qd, kd, 1u);
+          }
+        }
+        mma_commit(SFULL + 8 * sb);
+        for (int pp = 0; pp < KP; ++pp) mma_commit_mc(EMPTY(KSLOT(j, pp)));
       }
-      // arrives once every MMA this thread issued has completed; waited on before TMEM is freed
-      mma_commit(DRAIN);
+    } else {
+      const int BR = a.box_rows;
+      const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 512u;
+      for (int32_t jp = 0; ok && jp < ntiles; ++jp) {
+        const int pb = jp % NPB;
+        const int sidx = VSLOT(jp);
+        ok = wait1(FULL(sidx), (jp / NVR) & 1) && wait1(PFULL + 8 * pb, (jp / NPB) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vs = sSlots + sidx * kSlotBytes;
+        // V slot: page-major boxes of BR rows, each [4 chunks][BR rows][128 B]
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t key = 16u * kk;
+          const uint32_t va = vs + (key / BR) * (BR * 512u) + (key % BR) * 128u;
+          mma_ts<IDESC_PV>(tmem + kTmO, tmem + kTmP + pb * (kBN / 2) + kk * 8, sdesc(va, lbo, sbo),
+                           (jp > 0 || kk > 0) ? 1u : 0u);
+        }
+        if constexpr (C::SHARE_V) mma_commit_mc(EMPTY(sidx));
+        else mma_commit(EMPTY(sidx));
+        mma_commit(PVDONE + 8 * pb);
+      }
     }
+    // arrives once every MMA this warp issued has completed; waited on before TMEM is freed
+    mma_commit(DRAIN);
   } else if (warp >= 2 && warp <= 9) {
     // ------------------------------------------------------------ softmax + epilogue
     // Two warps per TMEM lane quarter: half h = 0 owns key columns [0,32) of each tile and
@@ -704,6 +791,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
   }
   __syncthreads();
+  // neither CTA of the pair leaves while the other may still multicast into it or arrive on
+  // its barriers
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -802,9 +892,24 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid(a.plan.num_work, a.pool.num_kv_heads, DQK / kDV);
-  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, tv, t);
+  // clusters of two: adjacent query tiles (head_dim 256; the plan pairs them) or the two
+  // output-column halves of a tile (head_dim 512)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.plan.num_work, a.pool.num_kv_heads, DQK / kDV);
+  cfg.blockDim = dim3(kThreadsTc, 1, 1);
+  cfg.dynamicSmemBytes = TcCfg<DQK>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = DQK == 256 ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = DQK == 256 ? 1 : 2;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (DQK == 256 && (a.plan.num_work & 1)) return cudaErrorInvalidValue;  // plan pairs the tiles
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<DQK>, tq, tkv, tv, t);
   count_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
