@@ -171,12 +171,12 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
-                                            uint32_t bar) {
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y,
@@ -198,12 +198,12 @@ __device__ __forceinline__ void cluster_sync() {
 }
 // TMA loads that land at the same shared-memory offset in both CTAs of the cluster pair and
 // complete transactions on the mbarrier at the same offset in each
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int x, int y,
-                                               uint32_t bar) {
+__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                               int c2, int c3, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y), "r"(bar), "h"((unsigned short)3)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "h"((unsigned short)3)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* tm, int x, int y,
@@ -426,11 +426,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (warp == 0 || (warp >= 10 && warp <= 12)) {
     // ------------------------------------------------------------ producers
-    // TMA throughput here is bounded by how fast one warp can issue copies, so four warps
-    // issue them: warps 0 and 10 load K (2-D boxes of BR rows x 64 d, one per lane, in the
-    // chunk-major 128B-swizzled layout QK's B operand needs), warps 11 and 12 load V (one
-    // 3-D box per page: BR rows x 256 d, landing page-major, which PV's MN-major B operand
-    // reads with a chunk stride of BR*128 bytes). Warp 0 also loads Q once.
+    // Four warps issue the copies, one box of BR key rows x 256 d per lane: warps 0 and 10
+    // load K, warps 11 and 12 load V (each warp every other box of a tile). K lands as
+    // [key / 8][64-d chunk][8 rows][128 B] (a 4-D box), so every 8-key atom of QK's K-major
+    // B operand sits 4096 bytes after the previous one across pages; V lands page-major as
+    // [chunk][BR rows][128 B] (a 3-D box), which PV's MN-major B operand reads with a chunk
+    // stride of BR*128 bytes. Warp 0 also loads Q once.
     const bool is_v = warp >= 11;
     const int pw = (warp == 0 || warp == 11) ? 0 : 1;   // which half of the tile's boxes
     const uint32_t FIX = bars + 8u * (C::NBAR - 4 + (warp == 0 ? 0 : warp - 9));
@@ -446,11 +447,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int BR = a.box_rows;          // key rows per box: min(page_size, 64)
     const int nbox = kBN / BR;          // boxes (pages or page parts) per 64-key tile
     const int64_t head_rows = (int64_t)ps;
-    // this warp's boxes: b = pw, pw + 2, ... (< nbox); K: one lane per (box, d chunk)
-    // lane -> (box, chunk): K lanes 4*i + c take box pw + 2*i, chunk c; V lanes i take box pw + 2*i
-    const int my_box = is_v ? pw + 2 * lane : pw + 2 * (lane >> 2);
-    const int my_chunk = is_v ? 0 : (lane & 3);
-    const bool box_lane = my_box < nbox && (is_v ? lane < 32 : true);
+    // this warp's boxes: lane i takes box pw + 2 i (< nbox)
+    const int my_box = pw + 2 * lane;
+    const bool box_lane = my_box < nbox;
     auto page_of = [&](int32_t t) -> int32_t {  // raw page id of this lane's box (-1: past kv_len)
       if (!box_lane) return -1;
       const int32_t ks = kb0 + t * kBN + my_box * BR;
@@ -469,7 +468,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const bool load = !past && !bad;
       // V rows past kv_len (partial last page) must read as zeros; K rows there are masked
       const bool fix = any_bad || (is_v && __any_sync(0xffffffffu, box_lane && kb + my_box * BR + BR > kv_len));
-      const uint32_t box_bytes = is_v ? (uint32_t)BR * 512u : (uint32_t)BR * 128u;
+      const uint32_t box_bytes = (uint32_t)BR * 512u;
       const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, load)) * box_bytes;
       const uint32_t slot = sSlots + s * kSlotBytes;
       const uint32_t bar = fix ? FIX : FULL(s);
@@ -487,8 +486,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (shared) tma_load_3d_mc(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
           else tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
         } else {
-          tma_load_2d_mc(slot + my_chunk * (kBN * 128) + my_box * (BR * 128), &tm_kv,
-                         d0 + my_chunk * 64, row, bar);
+          tma_load_4d_mc(slot + my_box * (BR * 512), &tm_kv, 0, 0, d0 / 64, row / 8, bar);
         }
       }
       if (fix) {
@@ -498,13 +496,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         // zero this warp's rows that must not be read: keys past kv_len, keys on bad pages
         for (int b = pw; b < nbox; b += 2) {
-          const int32_t pb = __shfl_sync(0xffffffffu, page, is_v ? (b - pw) / 2 : 4 * ((b - pw) / 2));
+          const int32_t pb = __shfl_sync(0xffffffffu, page, (b - pw) / 2);
           for (int r = 0; r < BR; ++r) {
             const int32_t key = kb + b * BR + r;
             if (key < kv_len && pb >= 0 && pb < a.num_pages) continue;
             const int c = lane >> 3, w16 = lane & 7;  // 4 chunks x 128 bytes = 32 lanes x 16 bytes
+            const int kt = b * BR + r;  // key within the tile
             const uint32_t off = is_v ? b * (BR * 512) + c * (BR * 128) + r * 128
-                                      : c * (kBN * 128) + (b * BR + r) * 128;
+                                      : (kt >> 3) * 4096 + c * 1024 + (kt & 7) * 128;
             *(reinterpret_cast<uint4*>(gbase + (slot - base) + off) + w16) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
@@ -565,15 +564,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_after();
         const uint32_t dS = tmem + kTmS + sb * kBN;
         // descriptors advance by 32 B per K step inside a 128-byte swizzle row and by one
-        // 64-column chunk (kBN or kM rows x 128 B) every 4 steps
-        const uint64_t kd0 = sdesc(kslot[0], 16, 1024);
+        // 64-column chunk every 4 steps: 1024 B in a K slot (8-key atoms 4096 B apart), kM x 128 B
+        // in Q
+        const uint64_t kd0 = sdesc(kslot[0], 16, 4096);
         // an opaque per-tile copy of Q's base descriptor keeps the compiler from hoisting all
         // 32 derived descriptors out of the loop (64 registers)
         uint64_t qd0 = sdesc(sQ, 16, 1024);
         asm volatile("mov.b64 %0, %0;" : "+l"(qd0));
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
           if constexpr (C::QT) {
             mma_ts<IDESC_QK>(dS, tmem + kTmQ + kk * 8, kd, kk > 0 ? 1u : 0u);
           } else {
@@ -582,11 +582,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
         if constexpr (KP > 1) {
-          const uint64_t kd1 = sdesc(kslot[KP - 1], 16, 1024);
+          const uint64_t kd1 = sdesc(kslot[KP - 1], 16, 4096);
 #pragma unroll
           for (int kk = 16; kk < 32; ++kk) {
             const int kin = kk & 15;
-            const uint64_t kd = kd1 + (uint64_t)(((kin >> 2) * (kBN * 128) + (kin & 3) * 32) >> 4);
+            const uint64_t kd = kd1 + (uint64_t)(((kin >> 2) * 1024 + (kin & 3) * 32) >> 4);
             const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
             mma_ss<IDESC_QK>(dS, qd, kd, 1u);
           }
@@ -840,12 +840,14 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   const int32_t ps = a.pool.page_size;
   const int32_t br = ps < 64 ? ps : 64;
   {
+    // K: dims (64 d, row within an 8-row group, d chunk, 8-row group); one box = br rows x
+    // 256 d of one page, landing as [group][chunk][8 rows][128 B]
     const cuuint64_t rows = (cuuint64_t)a.pool.num_pages * 2 * a.pool.num_kv_heads * ps;
-    cuuint64_t dims[2] = {(cuuint64_t)DQK, rows};
-    cuuint64_t strides[1] = {(cuuint64_t)DQK * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)br};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)a.pool.layer_base, dims, strides,
+    cuuint64_t dims[4] = {64, 8, (cuuint64_t)DQK / 64, rows / 8};
+    cuuint64_t strides[3] = {(cuuint64_t)DQK * 2, 128, (cuuint64_t)DQK * 2 * 8};
+    cuuint32_t box[4] = {64, 8, 4, (cuuint32_t)br / 8};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void*)a.pool.layer_base, dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
