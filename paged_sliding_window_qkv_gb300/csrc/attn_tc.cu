@@ -55,34 +55,31 @@ constexpr float kRescaleLog2 = 48.f;
 constexpr float kHeadroomLog2 = 64.f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// Two layouts, chosen by the contraction width:
-//  head_dim 256 (QT): Q lives in TMEM (QK reads A from TMEM like PV does), which frees shared
-//    memory for 7 ring slots (K 3 tiles, V 4 tiles). TMEM: O [0,256), Q [256,384),
-//    S [384,448) (one buffer), P [448,512) (two buffers). MMA order QK(j), PV(j-1), QK(j+1):
-//    the single S buffer is released as soon as the softmax has read it.
-//  head_dim 512: Q (128 KB) stays in shared memory; 3 ring slots (K 2 x 256 d, V 1).
-//    TMEM: O [0,256), S [256,384) (two buffers), P [384,480) (three buffers).
-//    MMA order QK(j), PV(j-2).
+// One TMEM map for both widths: O [0,256) (this CTA's 256 output columns), Q columns [0,256)
+// [256,384) (QK's first 256-d part reads A from TMEM), S [384,448) (one buffer, released as
+// soon as the softmax has read it), P [448,512) (two buffers). head_dim 512 keeps Q columns
+// [256,512) in shared memory (64 KB; QK's second part is SS). K streams through a ring of three
+// 256-d part slots (a tile is KP parts; a part's slot is released as soon as its 16 MMAs
+// complete), V through NVR tile slots; 7 slots for head_dim 256 (3 K + 4 V), 5 for 512 (3 + 2).
 template <int DQK>
 struct TcCfg {
-  static constexpr bool QT = DQK == 256;
-  static constexpr int KP = DQK / 256;          // K slots per tile (256 d each)
-  static constexpr int NKR = QT ? 3 : 1;        // tiles in the K ring
-  static constexpr int NVR = QT ? 4 : 1;        // tiles in the V ring
-  static constexpr int NS = NKR * KP + NVR;
-  static constexpr int Q_BYTES = QT ? 0 : kM * DQK * 2;
-  static constexpr int SMEM_DATA = Q_BYTES + NS * kSlotBytes;
+  static constexpr int KP = DQK / 256;                // K parts per tile (256 d each)
+  static constexpr int NKS = 3;                       // K part slots
+  static constexpr int NVR = DQK == 256 ? 4 : 2;      // V tile slots
+  static constexpr int NS = NKS + NVR;
+  static constexpr int QS_BYTES = (DQK - 256) * kM * 2;  // Q columns past 256, in shared memory
+  static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes;
   static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
   static constexpr int NBAR = 2 * NS + 21;      // ..., 4 per-producer fix-up barriers last
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
-  static constexpr int NSB = QT ? 1 : 2;        // S buffers
-  static constexpr int NPB = QT ? 2 : 3;        // P buffers
-  static constexpr int LAG = QT ? 1 : 2;        // PV(j - LAG) is issued after QK(j)
-  static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = QT ? 384 : 256, TM_P = QT ? 448 : 384;
+  static constexpr int NSB = 1;                 // S buffers
+  static constexpr int NPB = 2;                 // P buffers
+  static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384, TM_P = 448;
   // CTA pairs (clusters of two) share K/V loads by TMA multicast: head_dim 256 pairs two adjacent
   // query tiles (sharing K and V over their union key range); head_dim 512 pairs the two
   // output-column halves of one query tile (sharing K; each loads its own half of V)
-  static constexpr bool SHARE_V = QT;
+  static constexpr bool SHARE_V = DQK == 256;
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct TcArgs {
@@ -335,26 +332,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                const __grid_constant__ CUtensorMap tm_v, TcArgs a) {
   using C = TcCfg<DQK>;
-  constexpr int KP = C::KP, NKR = C::NKR, NVR = C::NVR, NS = C::NS;
-  constexpr int NSB = C::NSB, NPB = C::NPB, LAG = C::LAG;
+  constexpr int KP = C::KP, NKS = C::NKS, NVR = C::NVR, NS = C::NS;
+  constexpr int NSB = C::NSB, NPB = C::NPB;
   constexpr uint32_t kTmO = C::TM_O, kTmQ = C::TM_Q, kTmS = C::TM_S, kTmP = C::TM_P;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
-  const uint32_t sSlots = base + C::Q_BYTES;
+  const uint32_t sSlots = base + C::QS_BYTES;
   float* xl = reinterpret_cast<float*>(gbase + C::SMEM_DATA);  // [2 halves][128 rows]
   const uint32_t bars = base + C::SMEM_DATA + C::XL_BYTES;
   auto FULL = [&](int s) { return bars + 8u * s; };
   auto EMPTY = [&](int s) { return bars + 8u * (NS + s); };
   const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
-                 PVDONE = SFULL + 56, QFULL = SFULL + 80, FIXB = SFULL + 88,
-                 DRAIN = SFULL + 96, PAIRB = SFULL + 104,  // PAIRB: 4 barriers, one per lane quarter
-                 FIXV = SFULL + 136;
-  // ring slots: K slots of tile j, then V slot of tile j
-  auto KSLOT = [&](int32_t j, int pp) { return (int)(j % NKR) * KP + pp; };
-  auto VSLOT = [&](int32_t j) { return NKR * KP + (int)(j % NVR); };
+                 PVDONE = SFULL + 56, QFULL = SFULL + 80,
+                 DRAIN = SFULL + 96, PAIRB = SFULL + 104;  // PAIRB: 4 barriers, one per lane quarter
+  // ring slots: K part pp of tile j is the (j KP + pp)-th part through the NKS K slots; V
+  // tile j uses V slot j mod NVR
+  auto KSLOT = [&](int32_t j, int pp) { return (int)((j * KP + pp) % NKS); };
+  auto KROUND = [&](int32_t j, int pp) { return (int)((j * KP + pp) / NKS); };
+  auto VSLOT = [&](int32_t j) { return NKS + (int)(j % NVR); };
   uint32_t* tmem_slot =
       reinterpret_cast<uint32_t*>(gbase + C::SMEM_DATA + C::XL_BYTES + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -394,7 +392,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int s = 0; s < NS; ++s) {
       mbar_init(FULL(s), 2);
       // a shared slot is free again once both CTAs' MMAs have consumed it
-      mbar_init(EMPTY(s), (s < NKR * KP || C::SHARE_V) ? 2 : 1);
+      mbar_init(EMPTY(s), (s < NKS || C::SHARE_V) ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SFULL + 8 * b, 1);
@@ -404,9 +402,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(PFULL + 8 * b, 8);
       mbar_init(PVDONE + 8 * b, 1);
     }
-    mbar_init(QFULL, C::QT ? 8 : 1);  // QT: the eight softmax warps store Q into TMEM
-    mbar_init(FIXB, 1);
-    mbar_init(FIXV, 1);
+    // the eight softmax warps store Q columns [0,256) into TMEM; head_dim 512 also loads the
+    // rest by TMA
+    mbar_init(QFULL, C::QS_BYTES > 0 ? 9 : 8);
     for (int f = 0; f < 4; ++f) mbar_init(bars + 8u * (C::NBAR - 4 + f), 1);
     mbar_init(DRAIN, 2);  // one final commit from each MMA-issuing thread
     for (int q = 0; q < 4; ++q) mbar_init(PAIRB + 8 * q, 2);
@@ -437,11 +435,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t FIX = bars + 8u * (C::NBAR - 4 + (warp == 0 ? 0 : warp - 9));
     uint32_t fix_phase = 0;
     bool ok = true;
-    if (!C::QT && lane == 0 && warp == 0) {
+    if (C::QS_BYTES > 0 && lane == 0 && warp == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
-      mbar_expect_tx(QFULL, C::Q_BYTES);
-      for (int c = 0; c < DQK / 64; ++c)
-        tma_load_3d(sQ + c * (kM * 128), &tm_q, c * 64, g * G, q0 + tok0, QFULL);
+      mbar_expect_tx(QFULL, C::QS_BYTES);
+      for (int c = 0; c < (DQK - 256) / 64; ++c)
+        tma_load_3d(sQ + c * (kM * 128), &tm_q, 256 + c * 64, g * G, q0 + tok0, QFULL);
     }
     if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(is_v ? &tm_v : &tm_kv) : "memory");
     const int BR = a.box_rows;          // key rows per box: min(page_size, 64)
@@ -522,7 +520,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int32_t qn = t + kLook + 1 < ntiles ? page_of(t + kLook + 1) : -1;
       if (!is_v) {
         for (int pp = 0; ok && pp < KP; ++pp)
-          ok = issue_part(KSLOT(t, pp), (int)(t / NKR), pp * 256, t, qid[0]);
+          ok = issue_part(KSLOT(t, pp), KROUND(t, pp), pp * 256, t, qid[0]);
       } else {
         ok = issue_part(VSLOT(t), (int)(t / NVR), dh * 256, t, qid[0]);
       }
@@ -554,45 +552,40 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int32_t j = 0; ok && j < ntiles; ++j) {
         const int sb = j % NSB;
         ok = wait1(SFREE + 8 * sb, ((j / NSB) & 1) ^ 1);
-        uint32_t kslot[KP];
+        if (!ok) break;
+        const uint32_t dS = tmem + kTmS + sb * kBN;
         for (int pp = 0; ok && pp < KP; ++pp) {
           const int sidx = KSLOT(j, pp);
-          kslot[pp] = sSlots + sidx * kSlotBytes;
-          ok = wait1(FULL(sidx), (j / NKR) & 1);
+          ok = wait1(FULL(sidx), KROUND(j, pp) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          // descriptors advance by 32 B per K step inside a 128-byte swizzle row and by one
+          // 64-column chunk every 4 steps: 1024 B in a K slot (8-key atoms 4096 B apart),
+          // kM x 128 B in shared-memory Q
+          const uint64_t kd0 = sdesc(sSlots + sidx * kSlotBytes, 16, 4096);
+          if (pp == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
+              mma_ts<IDESC_QK>(dS, tmem + kTmQ + kk * 8, kd, kk > 0 ? 1u : 0u);
+            }
+          } else {
+            // an opaque copy of Q's base descriptor keeps the compiler from hoisting the 16
+            // derived descriptors out of the loop
+            uint64_t qd0 = sdesc(sQ, 16, 1024);
+            asm volatile("mov.b64 %0, %0;" : "+l"(qd0));
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
+              const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+              mma_ss<IDESC_QK>(dS, qd, kd, 1u);
+            }
+          }
+          // this part's slot is free once its MMAs (and all earlier ones) complete
+          mma_commit_mc(EMPTY(sidx));
         }
         if (!ok) break;
-        tc_fence_after();
-        const uint32_t dS = tmem + kTmS + sb * kBN;
-        // descriptors advance by 32 B per K step inside a 128-byte swizzle row and by one
-        // 64-column chunk every 4 steps: 1024 B in a K slot (8-key atoms 4096 B apart), kM x 128 B
-        // in Q
-        const uint64_t kd0 = sdesc(kslot[0], 16, 4096);
-        // an opaque per-tile copy of Q's base descriptor keeps the compiler from hoisting all
-        // 32 derived descriptors out of the loop (64 registers)
-        uint64_t qd0 = sdesc(sQ, 16, 1024);
-        asm volatile("mov.b64 %0, %0;" : "+l"(qd0));
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
-          if constexpr (C::QT) {
-            mma_ts<IDESC_QK>(dS, tmem + kTmQ + kk * 8, kd, kk > 0 ? 1u : 0u);
-          } else {
-            const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
-            mma_ss<IDESC_QK>(dS, qd, kd, kk > 0 ? 1u : 0u);
-          }
-        }
-        if constexpr (KP > 1) {
-          const uint64_t kd1 = sdesc(kslot[KP - 1], 16, 4096);
-#pragma unroll
-          for (int kk = 16; kk < 32; ++kk) {
-            const int kin = kk & 15;
-            const uint64_t kd = kd1 + (uint64_t)(((kin >> 2) * 1024 + (kin & 3) * 32) >> 4);
-            const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
-            mma_ss<IDESC_QK>(dS, qd, kd, 1u);
-          }
-        }
         mma_commit(SFULL + 8 * sb);
-        for (int pp = 0; pp < KP; ++pp) mma_commit_mc(EMPTY(KSLOT(j, pp)));
       }
     } else {
       const int BR = a.box_rows;
@@ -637,7 +630,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     constexpr int HC = kBN / 2;  // key columns per half
-    if constexpr (C::QT) {
+    {
       // Q rows into TMEM: this thread stores its row's d columns [128h, 128h + 128) as bf16
       // pairs (64 TMEM columns), the A operand layout of QK
       const uint4* src = reinterpret_cast<const uint4*>(
