@@ -56,8 +56,10 @@ constexpr float kHeadroomLog2 = 64.f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // One TMEM map for both widths: O [0,256) (this CTA's 256 output columns), Q columns [0,256)
-// [256,384) (QK's first 256-d part reads A from TMEM), S [384,448) (one buffer, released as
-// soon as the softmax has read it), P [448,512) (two buffers). head_dim 512 keeps Q columns
+// [256,384) (QK's first 256-d part reads A from TMEM), two S buffers [384,448) and [448,512).
+// P(j) (bf16 pairs, 32 columns) overwrites the first half of S(j) once both softmax warps of
+// a row have read it, and PV(j) reads it there, so QK(j) only waits for PV(j - 2) to have
+// consumed its buffer: QK runs ahead of the softmax by a tile. head_dim 512 keeps Q columns
 // [256,512) in shared memory (64 KB; QK's second part is SS). K streams through a ring of three
 // 256-d part slots (a tile is KP parts; a part's slot is released as soon as its 16 MMAs
 // complete), V through NVR tile slots; 7 slots for head_dim 256 (3 K + 4 V), 5 for 512 (3 + 2).
@@ -72,9 +74,8 @@ struct TcCfg {
   static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
   static constexpr int NBAR = 2 * NS + 21;      // ..., 4 per-producer fix-up barriers last
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
-  static constexpr int NSB = 1;                 // S buffers
-  static constexpr int NPB = 2;                 // P buffers
-  static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384, TM_P = 448;
+  static constexpr int NSB = 2;                 // S buffers (P aliased in them)
+  static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
   // CTA pairs (clusters of two) share K/V loads by TMA multicast: head_dim 256 pairs two adjacent
   // query tiles (sharing K and V over their union key range); head_dim 512 pairs the two
   // output-column halves of one query tile (sharing K; each loads its own half of V)
@@ -333,8 +334,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, TcArgs a) {
   using C = TcCfg<DQK>;
   constexpr int KP = C::KP, NKS = C::NKS, NVR = C::NVR, NS = C::NS;
-  constexpr int NSB = C::NSB, NPB = C::NPB;
-  constexpr uint32_t kTmO = C::TM_O, kTmQ = C::TM_Q, kTmS = C::TM_S, kTmP = C::TM_P;
+  constexpr int NSB = C::NSB;
+  constexpr uint32_t kTmO = C::TM_O, kTmQ = C::TM_Q, kTmS = C::TM_S;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -345,7 +346,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const uint32_t bars = base + C::SMEM_DATA + C::XL_BYTES;
   auto FULL = [&](int s) { return bars + 8u * s; };
   auto EMPTY = [&](int s) { return bars + 8u * (NS + s); };
-  const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
+  const uint32_t SFULL = bars + 8u * (2 * NS), PFULL = SFULL + 32,
                  PVDONE = SFULL + 56, QFULL = SFULL + 80,
                  DRAIN = SFULL + 96, PAIRB = SFULL + 104;  // PAIRB: 4 barriers, one per lane quarter
   // ring slots: K part pp of tile j is the (j KP + pp)-th part through the NKS K slots; V
@@ -396,7 +397,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SFULL + 8 * b, 1);
-      mbar_init(SFREE + 8 * b, 8);
     }
     for (int b = 0; b < 3; ++b) {
       mbar_init(PFULL + 8 * b, 8);
@@ -551,7 +551,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       ok = wait1(QFULL, 0);
       for (int32_t j = 0; ok && j < ntiles; ++j) {
         const int sb = j % NSB;
-        ok = wait1(SFREE + 8 * sb, ((j / NSB) & 1) ^ 1);
+        // S buffer sb is free once PV(j - 2) has read the P stored over S(j - 2)
+        ok = wait1(PVDONE + 8 * sb, ((j / NSB) & 1) ^ 1);
         if (!ok) break;
         const uint32_t dS = tmem + kTmS + sb * kBN;
         for (int pp = 0; ok && pp < KP; ++pp) {
@@ -591,9 +592,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int BR = a.box_rows;
       const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 512u;
       for (int32_t jp = 0; ok && jp < ntiles; ++jp) {
-        const int pb = jp % NPB;
+        const int pb = jp % NSB;
         const int sidx = VSLOT(jp);
-        ok = wait1(FULL(sidx), (jp / NVR) & 1) && wait1(PFULL + 8 * pb, (jp / NPB) & 1);
+        ok = wait1(FULL(sidx), (jp / NVR) & 1) && wait1(PFULL + 8 * pb, (jp / NSB) & 1);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vs = sSlots + sidx * kSlotBytes;
@@ -602,7 +603,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t key = 16u * kk;
           const uint32_t va = vs + (key / BR) * (BR * 512u) + (key % BR) * 128u;
-          mma_ts<IDESC_PV>(tmem + kTmO, tmem + kTmP + pb * (kBN / 2) + kk * 8, sdesc(va, lbo, sbo),
+          mma_ts<IDESC_PV>(tmem + kTmO, tmem + kTmS + pb * kBN + kk * 8, sdesc(va, lbo, sbo),
                            (jp > 0 || kk > 0) ? 1u : 0u);
         }
         if constexpr (C::SHARE_V) mma_commit_mc(EMPTY(sidx));
@@ -660,7 +661,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(SFREE + 8 * b);
+      if (lane == 0) mbar_arrive(pair_bar);  // this warp has read S(j)
       const int32_t kb = kb0 + j * kBN;
       const bool interior = __all_sync(0xffffffffu, rvalid && kb >= rlo && kb + kBN <= rhi);
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -701,7 +702,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         const int jp = j - 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp % NPB), (jp / NPB) & 1, abort_flag, a.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
         tc_fence_after();
         for (int c = 0; c < kDV / 64; ++c) {
           uint32_t o[32];
@@ -725,18 +726,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
       }
       l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      const int pb = j % NPB;
-      if (j >= NPB && !__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * pb, ((j / NPB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+      // P(j) overwrites the first half of S(j): the partner warp must have read S(j) as well
+      if (!__all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status))) { ok = false; break; }
+      pair_phase ^= 1u;
       tc_fence_after();
-      tmem_st16(tl + kTmP + pb * (kBN / 2) + h * (HC / 2), pk);
+      tmem_st16(tl + kTmS + b * kBN + h * (HC / 2), pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(PFULL + 8 * pb);
+      if (lane == 0) mbar_arrive(PFULL + 8 * b);
     }
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NPB), (jl / NPB) & 1, abort_flag, a.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, abort_flag, a.status));
     }
     // the row sum is the sum of both halves' partial sums
     if (ok) {
