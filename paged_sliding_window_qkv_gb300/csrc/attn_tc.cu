@@ -652,7 +652,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int32_t j = 0; ok && j < ntiles; ++j) {
       const int b = j % NSB;
-      if (!__all_sync(0xffffffffu, mbar_wait(SFULL + 8 * b, (j / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait_inline(SFULL + 8 * b, (j / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
       tc_fence_after();
       // both warps of the pair read the whole 64-key row: the row maximum needs no exchange
       uint32_t sv[kBN];
@@ -727,7 +727,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // P(j) overwrites the first half of S(j): the partner warp must have read S(j) as well
-      if (!__all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait_inline(pair_bar, pair_phase, abort_flag, a.status))) { ok = false; break; }
       pair_phase ^= 1u;
       tc_fence_after();
       tmem_st16(tl + kTmS + b * kBN + h * (HC / 2), pk);
