@@ -57,24 +57,28 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // One TMEM map for both widths: O [0,256) (this CTA's 256 output columns), Q columns [0,256)
 // [256,384) (QK's first 256-d part reads A from TMEM), two S buffers [384,448) and [448,512).
-// P(j) (bf16 pairs, 32 columns) overwrites the first half of S(j) once both softmax warps of
-// a row have read it, and PV(j) reads it there, so QK(j) only waits for PV(j - 2) to have
-// consumed its buffer: QK runs ahead of the softmax by a tile. head_dim 512 keeps Q columns
-// [256,512) in shared memory (64 KB; QK's second part is SS). K streams through a ring of three
-// 256-d part slots (a tile is KP parts; a part's slot is released as soon as its 16 MMAs
-// complete), V through NVR tile slots; 7 slots for head_dim 256 (3 K + 4 V), 5 for 512 (3 + 2).
+// head_dim 256 (P_SMEM): the softmax writes P(j) to one of two 16 KB shared-memory buffers
+// (PV is SS), so S(j)'s buffer is free as soon as the softmax has read it and QK(j + 2) waits
+// only for that. head_dim 512: P(j) (bf16 pairs, 32 columns) overwrites the first half of S(j)
+// once both softmax warps of a row have read it and PV(j) reads it there (TS), so QK(j + 2)
+// waits for PV(j); its shared memory instead holds Q columns [256,512) (64 KB; QK's second
+// part is SS). K streams through a ring of three 256-d part slots (a tile is KP parts; a
+// part's slot is released as soon as its 16 MMAs complete), V through NVR tile slots:
+// 6 slots for head_dim 256 (3 K + 3 V), 5 for 512 (3 + 2).
 template <int DQK>
 struct TcCfg {
   static constexpr int KP = DQK / 256;                // K parts per tile (256 d each)
   static constexpr int NKS = 3;                       // K part slots
-  static constexpr int NVR = DQK == 256 ? 4 : 2;      // V tile slots
+  static constexpr int NVR = DQK == 256 ? 3 : 2;      // V tile slots
   static constexpr int NS = NKS + NVR;
   static constexpr int QS_BYTES = (DQK - 256) * kM * 2;  // Q columns past 256, in shared memory
-  static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes;
+  static constexpr bool P_SMEM = DQK == 256;          // P in shared memory (else over S in TMEM)
+  static constexpr int P_BUF = kM * kBN * 2;          // one P buffer: 128 rows x 64 keys bf16
+  static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes + (P_SMEM ? 2 * P_BUF : 0);
   static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
   static constexpr int NBAR = 2 * NS + 21;      // ..., 4 per-producer fix-up barriers last
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
-  static constexpr int NSB = 2;                 // S buffers (P aliased in them)
+  static constexpr int NSB = 2;                 // S buffers (and P buffers)
   static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
   // CTA pairs (clusters of two) share K/V loads by TMA multicast: head_dim 256 pairs two adjacent
   // query tiles (sharing K and V over their union key range); head_dim 512 pairs the two
@@ -342,11 +346,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sSlots = base + C::QS_BYTES;
+  const uint32_t sP = sSlots + NS * kSlotBytes;  // P_SMEM: two P buffers
   float* xl = reinterpret_cast<float*>(gbase + C::SMEM_DATA);  // [2 halves][128 rows]
   const uint32_t bars = base + C::SMEM_DATA + C::XL_BYTES;
   auto FULL = [&](int s) { return bars + 8u * s; };
   auto EMPTY = [&](int s) { return bars + 8u * (NS + s); };
-  const uint32_t SFULL = bars + 8u * (2 * NS), PFULL = SFULL + 32,
+  const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
                  PVDONE = SFULL + 56, QFULL = SFULL + 80,
                  DRAIN = SFULL + 96, PAIRB = SFULL + 104;  // PAIRB: 4 barriers, one per lane quarter
   // ring slots: K part pp of tile j is the (j KP + pp)-th part through the NKS K slots; V
@@ -397,6 +402,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SFULL + 8 * b, 1);
+      mbar_init(SFREE + 8 * b, 8);  // P_SMEM: all softmax warps have read S
     }
     for (int b = 0; b < 3; ++b) {
       mbar_init(PFULL + 8 * b, 8);
@@ -551,8 +557,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       ok = wait1(QFULL, 0);
       for (int32_t j = 0; ok && j < ntiles; ++j) {
         const int sb = j % NSB;
-        // S buffer sb is free once PV(j - 2) has read the P stored over S(j - 2)
-        ok = wait1(PVDONE + 8 * sb, ((j / NSB) & 1) ^ 1);
+        // S buffer sb is free once the softmax has read S(j - 2) (P_SMEM), else once PV(j - 2)
+        // has read the P stored over it
+        ok = wait1((C::P_SMEM ? SFREE : PVDONE) + 8 * sb, ((j / NSB) & 1) ^ 1);
         if (!ok) break;
         const uint32_t dS = tmem + kTmS + sb * kBN;
         for (int pp = 0; ok && pp < KP; ++pp) {
@@ -603,8 +610,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t key = 16u * kk;
           const uint32_t va = vs + (key / BR) * (BR * 512u) + (key % BR) * 128u;
-          mma_ts<IDESC_PV>(tmem + kTmO, tmem + kTmS + pb * kBN + kk * 8, sdesc(va, lbo, sbo),
-                           (jp > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (C::P_SMEM) {
+            // P buffer: K-major, 128-byte swizzled rows of 64 keys; a K step is 32 bytes
+            mma_ss<IDESC_PV>(tmem + kTmO, sdesc(sP + pb * C::P_BUF + kk * 32, 16, 1024),
+                             sdesc(va, lbo, sbo), (jp > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            mma_ts<IDESC_PV>(tmem + kTmO, tmem + kTmS + pb * kBN + kk * 8, sdesc(va, lbo, sbo),
+                             (jp > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         if constexpr (C::SHARE_V) mma_commit_mc(EMPTY(sidx));
         else mma_commit(EMPTY(sidx));
@@ -661,7 +674,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pair_bar);  // this warp has read S(j)
+      // this warp has read S(j): P_SMEM frees the S buffer for QK(j + 2); otherwise the partner
+      // warp learns that P may now overwrite it
+      if (lane == 0) mbar_arrive(C::P_SMEM ? SFREE + 8 * b : pair_bar);
       const int32_t kb = kb0 + j * kBN;
       const bool interior = __all_sync(0xffffffffu, rvalid && kb >= rlo && kb + kBN <= rhi);
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -726,14 +741,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
       }
       l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      // P(j) overwrites the first half of S(j): the partner warp must have read S(j) as well
-      if (!__all_sync(0xffffffffu, mbar_wait_inline(pair_bar, pair_phase, abort_flag, a.status))) { ok = false; break; }
-      pair_phase ^= 1u;
-      tc_fence_after();
-      tmem_st16(tl + kTmS + b * kBN + h * (HC / 2), pk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
+      if constexpr (C::P_SMEM) {
+        // P buffer b is free once PV(j - 2) has read it
+        if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((j / NSB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+        // this row's 32 keys: four 16-byte chunks h*4 .. h*4+3 of its 128-byte row, at
+        // positions swizzled by the row within its 8-row atom
+        unsigned char* prow = gbase + (sP - base) + b * C::P_BUF + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(prow + (((h * 4 + c) ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_proxy_async();  // the PV MMA reads P through the async proxy
+        __syncwarp();
+      } else {
+        // P(j) overwrites the first half of S(j): the partner warp must have read S(j) as well
+        if (!__all_sync(0xffffffffu, mbar_wait_inline(pair_bar, pair_phase, abort_flag, a.status))) { ok = false; break; }
+        pair_phase ^= 1u;
+        tc_fence_after();
+        tmem_st16(tl + kTmS + b * kBN + h * (HC / 2), pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+      }
       if (lane == 0) mbar_arrive(PFULL + 8 * b);
     }
     if (ok && ntiles > 0) {
