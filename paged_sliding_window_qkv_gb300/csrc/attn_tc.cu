@@ -80,10 +80,6 @@ struct TcCfg {
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
   static constexpr int NSB = 2;                 // S buffers (and P buffers)
   static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
-  // CTA pairs (clusters of two) share K/V loads by TMA multicast: head_dim 256 pairs two adjacent
-  // query tiles (sharing K and V over their union key range); head_dim 512 pairs the two
-  // output-column halves of one query tile (sharing K; each loads its own half of V)
-  static constexpr bool SHARE_V = DQK == 256;
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -190,32 +186,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
-}
-// TMA loads that land at the same shared-memory offset in both CTAs of the cluster pair and
-// complete transactions on the mbarrier at the same offset in each
-__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
-                                               int c2, int c3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
-      "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "h"((unsigned short)3)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* tm, int x, int y,
-                                               int z, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar), "h"((unsigned short)3)
-      : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -253,14 +223,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
       "{\n .reg .pred e, p;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n setp.ne.b32 p, %3, 0;\n"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n}\n" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(acc), "n"(IDESC)
-      : "memory");
-}
-// arrive on the mbarrier at this offset in both CTAs of the pair once prior MMAs complete
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar) {
-  asm volatile(
-      "{\n .reg .pred e;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n}\n" ::"r"(bar), "h"((unsigned short)3)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -377,28 +339,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int32_t kv_len = (kvp1 - kvp0 - 1) * ps + pl.last_page_len[r];
   const int32_t sp = pl.start_pos[r];
   const int32_t W = a.window_left;
-  const uint32_t rank = cluster_rank();
-  // key range: this tile's visible keys, widened to the pair's union when the pair shares V
-  int32_t lo, hi;
-  {
-    const int32_t p_first = sp + tok0, p_last = sp + tok0 + ntok - 1;
-    lo = W >= 0 ? max(0, p_first - W) : 0;
-    hi = min(p_last + 1, kv_len);
-    if constexpr (C::SHARE_V) {
-      const int32_t pt0 = pl.work_tok0[item ^ 1];  // partner: same request, adjacent tile
-      const int32_t pn = min(a.cta_tile_q, pl.qo_indptr[r + 1] - q0 - pt0);
-      lo = min(lo, W >= 0 ? max(0, sp + pt0 - W) : 0);
-      hi = max(hi, min(sp + pt0 + pn, kv_len));
-    }
-  }
+  // key range: the keys some row of this tile sees
+  const int32_t p_first = sp + tok0, p_last = sp + tok0 + ntok - 1;
+  const int32_t lo = W >= 0 ? max(0, p_first - W) : 0;
+  const int32_t hi = min(p_last + 1, kv_len);
   const int32_t kb0 = lo & ~(kBN - 1);
   const int32_t ntiles = hi > kb0 ? (hi - kb0 + kBN - 1) / kBN : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(FULL(s), 2);
-      // a shared slot is free again once both CTAs' MMAs have consumed it
-      mbar_init(EMPTY(s), (s < NKS || C::SHARE_V) ? 2 : 1);
+      mbar_init(EMPTY(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SFULL + 8 * b, 1);
@@ -423,8 +374,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
-  // the peer's barriers must be initialised before any multicast copy or commit reaches them
-  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -481,16 +430,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         else if (!fix) mbar_arrive(bar);
       }
       __syncwarp();
-      // shared parts: the two CTAs split this warp's boxes and multicast them to both
-      const bool shared = !is_v || C::SHARE_V;
-      if (load && (!shared || (uint32_t)((my_box >> 1) & 1) == rank)) {
+      if (load) {
         const int32_t row = (int32_t)((((int64_t)page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + g) *
                                           head_rows + ((kb + my_box * BR) % ps));
         if (is_v) {
-          if (shared) tma_load_3d_mc(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
-          else tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
+          tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
         } else {
-          tma_load_4d_mc(slot + my_box * (BR * 512), &tm_kv, 0, 0, d0 / 64, row / 8, bar);
+          tma_load_4d(slot + my_box * (BR * 512), &tm_kv, 0, 0, d0 / 64, row / 8, bar);
         }
       }
       if (fix) {
@@ -590,7 +536,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
           }
           // this part's slot is free once its MMAs (and all earlier ones) complete
-          mma_commit_mc(EMPTY(sidx));
+          mma_commit(EMPTY(sidx));
         }
         if (!ok) break;
         mma_commit(SFULL + 8 * sb);
@@ -619,8 +565,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                              (jp > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        if constexpr (C::SHARE_V) mma_commit_mc(EMPTY(sidx));
-        else mma_commit(EMPTY(sidx));
+        mma_commit(EMPTY(sidx));
         mma_commit(PVDONE + 8 * pb);
       }
     }
@@ -815,9 +760,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
   }
   __syncthreads();
-  // neither CTA of the pair leaves while the other may still multicast into it or arrive on
-  // its barriers
-  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -918,22 +860,10 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  // clusters of two: adjacent query tiles (head_dim 256; the plan pairs them) or the two
-  // output-column halves of a tile (head_dim 512)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.plan.num_work, a.pool.num_kv_heads, DQK / kDV);
-  cfg.blockDim = dim3(kThreadsTc, 1, 1);
-  cfg.dynamicSmemBytes = TcCfg<DQK>::SMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = DQK == 256 ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = DQK == 256 ? 1 : 2;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (DQK == 256 && (a.plan.num_work & 1)) return cudaErrorInvalidValue;  // plan pairs the tiles
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<DQK>, tq, tkv, tv, t);
+  // one CTA per (query tile, KV head, 256-column half of the output)
+  const dim3 grid(a.plan.num_work, a.pool.num_kv_heads, DQK / kDV);
+  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, tv, t);
+  e = cudaSuccess;
   count_launch();
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -138,21 +138,12 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   const int32_t chunk = plan_kv_chunk(D);
   int64_t nwork = 0;
   std::vector<int32_t> wreq, wtok;
-  // The head_dim-256 tensor-memory kernel runs query tiles in pairs of adjacent tiles of one
-  // request (a CTA pair sharing K/V loads); a request with an odd tile count gets an empty
-  // partner item (first token = qo_len: no query rows).
-  const bool pair_tiles = D == 256 && plan_cta_tile_q(D, group, ps) == 128 / group;
   if (cta > 0) {
     for (int32_t r = 0; r < num_req; ++r) {
       const int32_t len = qo[r + 1] - qo[r];
-      int32_t n = 0;
-      for (int32_t t = 0; t < len; t += cta, ++n) {
+      for (int32_t t = 0; t < len; t += cta) {
         wreq.push_back(r);
         wtok.push_back(t);
-      }
-      if (pair_tiles && (n & 1)) {
-        wreq.push_back(r);
-        wtok.push_back(len);
       }
     }
     nwork = (int64_t)wreq.size();
