@@ -9,25 +9,26 @@
 // in shared memory) and walks the 64-key tiles of its visible key range, skipping
 // tiles outside the causal window.
 //
-//   warps 0, 10..12 producers (TMA): Q once; K (warps 0, 10) as 2-D boxes of page rows x
-//               64 d (chunk-major); V (warps 11, 12) as one 3-D box per page (page-major);
-//               separate K and V rings of 32 KB slots, 128B-swizzled;
-//   warps 1, 13 MMA issuers (one thread each): S = Q K^T into TMEM (M=128, N=64, K=16
-//               steps; warp 1) and O += P V with P read from TMEM (M=128, N=256, K=16
-//               steps; warp 13); completion is signalled with tcgen05.commit;
-//   warps 2..9  softmax: two threads per query row (each reads the whole S row for the
-//               maximum, exponentiates half of the tile's keys and owns half of O's
-//               columns), S read from TMEM, masked on boundary tiles only, online
-//               softmax in log2 units with lazy rescaling (O is rescaled in TMEM only
-//               when a row maximum outgrows a 2^64 headroom by more than 2^48: bf16 P and
-//               fp32 O and row sums hold the range, and O / l is unchanged), P written back
-//               to TMEM as bf16;
-//               then the epilogue normalises O and stores bf16 rows.
+//   warp 0     K producer (TMA): one 4-D box per page (BR rows x 256 d) into a ring of
+//              three 32 KB part slots; also Q columns [256,512) once (head_dim 512)
+//   warp 10    V producer (TMA): one 3-D box per page into NVR 32 KB slots
+//   warp 1     QK issuer: S = Q K^T into a TMEM S buffer (M=128, N=64, K=16 steps; the
+//              first 256-d part reads Q from TMEM, head_dim 512's second part from shared
+//              memory)
+//   warp 11    PV issuer: O += P V into TMEM (M=128, N=256, K=16 steps; P from shared
+//              memory for head_dim 256, from TMEM over S for head_dim 512); MMAs are issued
+//              by lane 0, completion signalled with tcgen05.commit
+//   warps 2..9 softmax: first Q columns [0,256) into TMEM; then two threads per query row
+//              (each reads the whole S row for the maximum, exponentiates half of the tile's
+//              keys and owns half of O's columns), masked on boundary tiles only, online
+//              softmax in log2 units with lazy rescaling (O is rescaled in TMEM only when a
+//              row maximum outgrows a 2^64 headroom by more than 2^48: bf16 P and fp32 O and
+//              row sums hold the range, and O / l is unchanged); then the epilogue
+//              normalises O and writes bf16 rows (full tiles staged in shared memory and
+//              written by TMA stores).
 //
-// TMEM (512 columns): O [0,256) fp32, S double buffer [256,384), P triple buffer
-// [384,480), per-row exchange between the two softmax warps of a lane quarter [480,488).
-// O holds 256 output columns: for head_dim 512 each query tile runs as two
-// CTAs (grid z), each computing the full 512-wide S and half of O.
+// O holds 256 output columns: for head_dim 512 each query tile runs as two CTAs (grid z),
+// each computing the full 512-wide S and half of O. The TMEM map is described at TcCfg.
 //
 // Every wait is bounded (two seconds of %globaltimer); a wait that runs out sets the
 // device status word, makes the CTA drain and free its tensor memory, and return.
@@ -46,7 +47,7 @@ constexpr int kM = 128;            // query rows per CTA
 constexpr int kBN = 64;            // keys per KV tile
 constexpr int kDV = 256;           // output columns per CTA
 constexpr int kSlotBytes = kBN * 256 * 2;  // 64 keys x 256 d bf16 = 32 KB
-constexpr int kThreadsTc = 448;  // producers 0,10..12; QK issuer 1; PV issuer 13; softmax 2..9
+constexpr int kThreadsTc = 384;  // K producer 0; QK issuer 1; softmax 2..9; V producer 10; PV issuer 11
 // Lazy rescaling: a row's reference maximum is set 2^64 above the first maximum it sees and
 // O is rescaled only when a later maximum exceeds the reference by more than 2^48. P stays
 // within [2^-64, 2^48] of the row's true maximum weight: inside bf16's and fp32's range, with
@@ -186,6 +187,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+// TMA store of a 3-D box from shared memory, and the bulk-group commit / wait for its reads
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tm),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -297,7 +312,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 template <int DQK>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-               const __grid_constant__ CUtensorMap tm_v, TcArgs a) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               TcArgs a) {
   using C = TcCfg<DQK>;
   constexpr int KP = C::KP, NKS = C::NKS, NVR = C::NVR, NS = C::NS;
   constexpr int NSB = C::NSB;
@@ -314,7 +330,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   auto FULL = [&](int s) { return bars + 8u * s; };
   auto EMPTY = [&](int s) { return bars + 8u * (NS + s); };
   const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
-                 PVDONE = SFULL + 56, QFULL = SFULL + 80,
+                 PVDONE = SFULL + 56, QFULL = SFULL + 80, EPIB = SFULL + 88,
                  DRAIN = SFULL + 96, PAIRB = SFULL + 104;  // PAIRB: 4 barriers, one per lane quarter
   // ring slots: K part pp of tile j is the (j KP + pp)-th part through the NKS K slots; V
   // tile j uses V slot j mod NVR
@@ -348,7 +364,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(FULL(s), 2);
+      mbar_init(FULL(s), 1);
       mbar_init(EMPTY(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -364,6 +380,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_init(QFULL, C::QS_BYTES > 0 ? 9 : 8);
     for (int f = 0; f < 4; ++f) mbar_init(bars + 8u * (C::NBAR - 4 + f), 1);
     mbar_init(DRAIN, 2);  // one final commit from each MMA-issuing thread
+    mbar_init(EPIB, 8);   // the softmax warps have staged their output rows
     for (int q = 0; q < 4; ++q) mbar_init(PAIRB + 8 * q, 2);
     *abort_flag = 0;
     fence_barrier_init();
@@ -377,17 +394,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 || (warp >= 10 && warp <= 12)) {
+  if (warp == 0 || warp == 10) {
     // ------------------------------------------------------------ producers
-    // Four warps issue the copies, one box of BR key rows x 256 d per lane: warps 0 and 10
-    // load K, warps 11 and 12 load V (each warp every other box of a tile). K lands as
+    // Two warps issue the copies, one box of BR key rows x 256 d per lane: warp 0 loads K,
+    // warp 10 loads V. K lands as
     // [key / 8][64-d chunk][8 rows][128 B] (a 4-D box), so every 8-key atom of QK's K-major
     // B operand sits 4096 bytes after the previous one across pages; V lands page-major as
     // [chunk][BR rows][128 B] (a 3-D box), which PV's MN-major B operand reads with a chunk
     // stride of BR*128 bytes. Warp 0 also loads Q once.
-    const bool is_v = warp >= 11;
-    const int pw = (warp == 0 || warp == 11) ? 0 : 1;   // which half of the tile's boxes
-    const uint32_t FIX = bars + 8u * (C::NBAR - 4 + (warp == 0 ? 0 : warp - 9));
+    const bool is_v = warp == 10;
+    const uint32_t FIX = bars + 8u * (C::NBAR - 4 + (is_v ? 1 : 0));
     uint32_t fix_phase = 0;
     bool ok = true;
     if (C::QS_BYTES > 0 && lane == 0 && warp == 0) {
@@ -400,8 +416,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int BR = a.box_rows;          // key rows per box: min(page_size, 64)
     const int nbox = kBN / BR;          // boxes (pages or page parts) per 64-key tile
     const int64_t head_rows = (int64_t)ps;
-    // this warp's boxes: lane i takes box pw + 2 i (< nbox)
-    const int my_box = pw + 2 * lane;
+    // lane i takes box i of the tile (< nbox)
+    const int my_box = lane;
     const bool box_lane = my_box < nbox;
     auto page_of = [&](int32_t t) -> int32_t {  // raw page id of this lane's box (-1: past kv_len)
       if (!box_lane) return -1;
@@ -445,8 +461,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           fix_phase ^= 1u;
         }
         // zero this warp's rows that must not be read: keys past kv_len, keys on bad pages
-        for (int b = pw; b < nbox; b += 2) {
-          const int32_t pb = __shfl_sync(0xffffffffu, page, (b - pw) / 2);
+        for (int b = 0; b < nbox; ++b) {
+          const int32_t pb = __shfl_sync(0xffffffffu, page, b);
           for (int r = 0; r < BR; ++r) {
             const int32_t key = kb + b * BR + r;
             if (key < kv_len && pb >= 0 && pb < a.num_pages) continue;
@@ -487,9 +503,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       while (globaltimer() - t0 < 100000ull) {
       }
     }
-  } else if (warp == 1 || warp == 13) {
+  } else if (warp == 1 || warp == 11) {
     // ------------------------------------------------------------ MMA issuers
-    // QK (warp 1) and PV (warp 13) are issued by two warps; they accumulate into disjoint
+    // QK (warp 1) and PV (warp 11) are issued by two warps; they accumulate into disjoint
     // TMEM (S and O) and are ordered against each other only through the barriers. Lane 0
     // waits on the barriers and issues; the other lanes follow it through the loop.
     constexpr uint32_t IDESC_QK = idesc_bf16(kM, kBN, false);
@@ -726,26 +742,58 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = a.out + ((int64_t)(q0 + tok0 + row / G) * Hq + g * G + row % G) * DQK +
-                           dh * kDV + h * (kDV / 2);
-      for (int c = 0; c < kDV / 64; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tl + kTmO + h * (kDV / 2) + c * 32, o);
-        tmem_wait_ld();
-        if (ntiles == 0) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (rvalid) {
+      if (ntok == a.cta_tile_q) {
+        // a full tile: stage the 128 x 256 output in the (now idle) ring slots as four 64-column
+        // 128-byte-swizzled boxes and write them with TMA stores
+        for (int c = 0; c < kDV / 64; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tl + kTmO + h * (kDV / 2) + c * 32, o);
+          tmem_wait_ld();
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+            w[e] = ntiles == 0 ? 0u
+                               : pack_bf16(__uint_as_float(o[2 * e]) * inv,
+                                           __uint_as_float(o[2 * e + 1]) * inv);
+          const int box = h * 2 + (c >> 1), piece0 = (c & 1) * 4;
+          unsigned char* rowp = gbase + (sSlots - base) + box * (kM * 128) + row * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(rowp + (((piece0 + k) ^ (row & 7)) << 4)) =
+                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        }
+        fence_proxy_async();  // the TMA store reads the staged rows through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(EPIB);
+        if (warp == 2 && lane == 0 && mbar_wait(EPIB, 0, abort_flag, a.status)) {
+          for (int bx = 0; bx < kDV / 64; ++bx)
+            tma_store_3d(&tm_o, sSlots + bx * (kM * 128), dh * kDV + bx * 64, g * G, q0 + tok0);
+          bulk_commit();
+          bulk_wait_read();  // the staged rows must be read before the CTA's memory is released
+        }
+      } else {
+        // a partial tile (the request's last): rows past its tokens belong to the next request
+        __nv_bfloat16* dst = a.out + ((int64_t)(q0 + tok0 + row / G) * Hq + g * G + row % G) * DQK +
+                             dh * kDV + h * (kDV / 2);
+        for (int c = 0; c < kDV / 64; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tl + kTmO + h * (kDV / 2) + c * 32, o);
+          tmem_wait_ld();
+          if (ntiles == 0) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          if (rvalid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
+            d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          }
         }
       }
     }
@@ -791,14 +839,16 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int32_t G = a.group, TQ = a.cta_tile_q;
-  CUtensorMap tq, tkv, tv;
-  {
+  CUtensorMap tq, tkv, tv, to;
+  // Q and the output share one shape: dims (d, head, token); a box is 64 d x G heads x TQ tokens
+  for (int m = 0; m < 2; ++m) {
     cuuint64_t dims[3] = {(cuuint64_t)DQK, (cuuint64_t)a.num_qo_heads,
                           (cuuint64_t)a.plan.num_tokens};
     cuuint64_t strides[2] = {(cuuint64_t)DQK * 2, (cuuint64_t)a.num_qo_heads * DQK * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
     cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.q, dims, strides, box, es,
+    if (enc(m == 0 ? &tq : &to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            m == 0 ? (void*)a.q : (void*)a.out, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -862,7 +912,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   }
   // one CTA per (query tile, KV head, 256-column half of the output)
   const dim3 grid(a.plan.num_work, a.pool.num_kv_heads, DQK / kDV);
-  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, tv, t);
+  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, tv, to, t);
   e = cudaSuccess;
   count_launch();
   if (e != cudaSuccess) return e;
