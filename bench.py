@@ -302,13 +302,17 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     launches0 = pg.pg_launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     for k in range(args.steps):
+        # the flush is queued ahead of the step (no host sync in between), so the step's first
+        # event does not also time the host's launch of its first call
         flush.zero_()
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
         step(all_evs[k])
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     launches = pg.pg_launch_count() - launches0
     clocks = sampler.stop()
     assert pg.pg_device_status() == pg.PG_OK

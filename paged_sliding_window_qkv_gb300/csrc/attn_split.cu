@@ -72,9 +72,10 @@ __device__ __forceinline__ uint32_t swz(int m, int c) {
   return (uint32_t)(m * (D * 2) + ((c ^ (m & 7)) << 4));
 }
 
-template <int D_, int BM_, int BN_, int NT_, int KS_, bool DECODE_>
+template <int D_, int BM_, int BN_, int NT_, int KS_, bool DECODE_, int NS_ = 2>
 struct Cfg {
   static constexpr int D = D_, BM = BM_, BN = BN_, NT = NT_, KS = KS_;
+  static constexpr int NS = NS_;  // K/V tile stages: NS - 1 tiles in flight while one computes
   static constexpr bool DECODE = DECODE_;
   static constexpr int CH = D / 8;                 // 16-byte chunks per row
   // S = Q K^T warp tiling: (BM/16) m-tiles x (BN/8/NT) n-groups x KS k-splits = 8 warps
@@ -96,7 +97,8 @@ struct Cfg {
   static constexpr size_t KV_BYTES = (size_t)BN * D * 2;
   static constexpr size_t S_BYTES = (size_t)KS * BM * SLD * 4;
   static constexpr size_t P_BYTES = (size_t)BM * PLD * 2;
-  static constexpr size_t SMEM = Q_BYTES + 4 * KV_BYTES + S_BYTES + P_BYTES + 2 * BM * 4;
+  static constexpr size_t SMEM = Q_BYTES + 2 * NS * KV_BYTES + S_BYTES + P_BYTES + 2 * BM * 4;
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 template <class C>
@@ -105,9 +107,9 @@ attn_split_kernel(AttnArgs a) {
   constexpr int D = C::D, BM = C::BM, BN = C::BN;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* sQ = smem;
-  unsigned char* sK = sQ + C::Q_BYTES;               // 2 stages
-  unsigned char* sV = sK + 2 * C::KV_BYTES;          // 2 stages
-  float* sS = reinterpret_cast<float*>(sV + 2 * C::KV_BYTES);
+  unsigned char* sK = sQ + C::Q_BYTES;               // NS stages
+  unsigned char* sV = sK + C::NS * C::KV_BYTES;      // NS stages
+  float* sS = reinterpret_cast<float*>(sV + C::NS * C::KV_BYTES);
   __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<unsigned char*>(sS) + C::S_BYTES);
   float* sAlpha = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sP) + C::P_BYTES);
   float* sL = sAlpha + BM;
@@ -183,8 +185,14 @@ attn_split_kernel(AttnArgs a) {
   };
 
   const int32_t ntiles = (hi - lo + BN - 1) / BN;
+  // the first NS - 1 tiles (one commit group each; Q rides in the first)
   load_kv(0, lo);
   cp_async_commit();
+#pragma unroll
+  for (int st = 1; st < C::NS - 1; ++st) {
+    if (st < ntiles) load_kv(st, lo + st * BN);
+    cp_async_commit();
+  }
 
   // S-warp coordinates
   const int s_mt = warp % C::WM;
@@ -205,11 +213,13 @@ attn_split_kernel(AttnArgs a) {
   for (int i = 0; i < C::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
   for (int32_t it = 0; it < ntiles; ++it) {
-    const int stage = it & 1;
+    const int stage = it % C::NS;
     const int32_t kb = lo + it * BN;
-    cp_async_wait<0>();
+    // tile it has landed (at most NS - 2 newer groups pending); every warp is past tile it - 1,
+    // whose stage the next load reuses
+    cp_async_wait<C::NS - 2>();
     __syncthreads();
-    if (it + 1 < ntiles) load_kv(stage ^ 1, kb + BN);
+    if (it + C::NS - 1 < ntiles) load_kv((it + C::NS - 1) % C::NS, kb + (C::NS - 1) * BN);
     cp_async_commit();
 
     // ---- S = Q K^T (this warp: one m-tile, NT n-tiles, one k-split) ----
@@ -407,6 +417,8 @@ attn_merge_kernel(AttnArgs a) {
 
 using Pre256 = Cfg<256, 64, 32, 2, 1, false>;
 using Pre512 = Cfg<512, 32, 32, 1, 1, false>;
+// decode: deeper stage rings (Cfg's NS) measured no faster; the per-tile chain of the CTA,
+// not the loads in flight, bounds these shapes
 using Dec256 = Cfg<256, 16, 32, 1, 2, true>;
 using Dec512 = Cfg<512, 16, 32, 1, 2, true>;
 

@@ -2,30 +2,35 @@
 // RMSNorm on V (never rotated), with K and V scattered straight into the layer's paged
 // pool ("gemma4: serving prep needs pool-write forms", Description and Proposed Plan).
 //
-// HBM-bound single pass. One CTA per token row; each warp owns whole head rows so the
-// RMS reduction is a warp shuffle. Every lane moves 16-byte vectors; a head row of
-// 256 bf16 is one 512-byte coalesced access per warp, a 512-wide row two of them.
-// All loads of a warp's rows are issued before any arithmetic so each warp keeps
-// several 512-byte requests in flight.
+// HBM-bound single pass, one persistent CTA per (SM, slot) walking the tokens
+// t = blockIdx.x + k * gridDim.x. A producer warp streams each token's raw rows (all of its
+// Q rows, K rows and V rows are contiguous runs) and its rotary row into a ring of
+// shared-memory stages with bulk asynchronous copies (cp.async.bulk, completion counted in
+// bytes on the stage's mbarrier), several tokens ahead, so every SM keeps hundreds of KB of
+// loads in flight without holding them in registers. Eight consumer warps each own whole
+// head rows of the staged token: a lane reads 16-byte vectors from shared memory (a 256-wide
+// row is one conflict-free 512-byte read per warp), the RMS reduction is a warp shuffle, the
+// hd256 rotary partner lives in lane ^ 16 and the hd512 partner in the same lane, and every
+// result row is one coalesced 512-byte (or 1 KB) store: q_out rows, or K/V rows at the
+// token's paged slot. The producer also resolves each token's request, position and page
+// (32 tokens at a time, one per lane) and passes them to the consumers in the stage header.
+//
+// Waits are bounded (two seconds of %globaltimer); a wait that runs out sets the device
+// status word and the CTA leaves the loop. Tokens whose metadata is out of range set the
+// status word and are skipped (no copy, no store).
 #include "pg_internal.h"
 
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
+
 namespace pg {
 namespace {
 
-struct alignas(16) V8 {
-  uint4 u;
-};
-
-__device__ __forceinline__ uint4 ld_stream(const __nv_bfloat16* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+constexpr int kPrepConsumerWarps = 8;
+constexpr int kPrepThreads = (kPrepConsumerWarps + 1) * 32;  // + producer warp
+constexpr uint64_t kPrepWaitNs = 2000000000ull;
 
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -52,16 +57,67 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ void set_status(int* st) { atomicOr(st, kStatusBounds); }
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of the given parity; false when it (or another warp) gave up.
+__device__ __noinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      int* status) {
+  if (bar_try(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  while (!bar_try(bar, parity)) {
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kPrepWaitNs) {
+      atomicOr(status, kStatusTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+// global -> shared bulk copy whose bytes complete on `bar`
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 
-// Per-token addressing shared by both forms. Returns false (and flags the status word)
-// when metadata would put the access out of range.
-struct TokenSlot {
-  int32_t pos;
-  __nv_bfloat16* k_row0;  // K row of kv head 0 at this token's slot (V is +stride_kv)
+// Token metadata the consumers need, written by the producer into the stage header.
+struct alignas(16) TokMeta {
+  int64_t slot;  // element offset of the token's K row of kv head 0 in the layer
+  int32_t pos;   // absolute position (rotary row)
+  int32_t ok;    // 0: out-of-range metadata, token skipped
 };
 
-__device__ __forceinline__ bool token_slot(const PrepArgs& a, int32_t t, TokenSlot* ts) {
+// Request, position and paged slot of token t, with every index checked before use.
+__device__ __forceinline__ bool token_meta(const PrepArgs& a, int32_t t, TokMeta* m) {
   const PlanDev& pl = a.plan;
   const int32_t r = pl.tok_req[t];
   if (r < 0 || r >= pl.num_req) return false;
@@ -74,186 +130,231 @@ __device__ __forceinline__ bool token_slot(const PrepArgs& a, int32_t t, TokenSl
     return false;
   const int32_t page = pl.page_ids[pidx];
   if (page < 0 || page >= a.pool.num_pages) return false;
-  ts->pos = pos;
-  ts->k_row0 = a.pool.layer_base + (int64_t)page * a.pool.stride_page +
-               (int64_t)(pos % ps) * a.pool.head_dim;
+  m->pos = pos;
+  m->slot = (int64_t)page * a.pool.stride_page + (int64_t)(pos % ps) * a.pool.head_dim;
+  m->ok = 1;
   return true;
 }
 
-// ----------------------------------------------------------------------------- hd256
-// Lane l holds elements [8l, 8l+8) of a 256-wide row; its rotary partner elements
-// (i +/- 128) live in lane l ^ 16. Rows of a token: Hq query rows, then Hkv K rows,
-// then Hkv V rows.
-constexpr int kWarps256 = 8;
-constexpr int kMaxRows256 = 4;  // rows per warp held in registers per pass
-
-__global__ void __launch_bounds__(kWarps256 * 32)
-prep_hd256_kernel(PrepArgs a) {
-  const int32_t t = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int32_t Hq = a.num_qo_heads;
-  const int32_t Hkv = a.pool.num_kv_heads;
-  const int32_t nrows = Hq + 2 * Hkv;
-
-  TokenSlot ts;
-  const bool ok = token_slot(a, t, &ts);
-  if (!ok) {
-    if (threadIdx.x == 0) set_status(a.status);
-    return;
-  }
-  const int half = lane >> 4;      // 0: elements [0,128), 1: [128,256)
-  const int ci = (lane & 15) * 8;  // rotary table column of this lane's first element
-  float c[8], s[8];
-  {
-    const float4* cp = reinterpret_cast<const float4*>(a.rope_cos + (int64_t)ts.pos * 128 + ci);
-    const float4* sp = reinterpret_cast<const float4*>(a.rope_sin + (int64_t)ts.pos * 128 + ci);
-    float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
-    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-    s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-  }
-  float wq[8], wk[8];
-  unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_q) + lane), wq);
-  unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_k) + lane), wk);
-
-  for (int base = warp; base < nrows; base += kWarps256 * kMaxRows256) {
-    uint4 raw[kMaxRows256];
+// Normalise (and for Q/K rows weight and rotate) one staged row and store it.
+//   D = 256: lane l holds elements [8l, 8l + 8); its rotary partners (i -/+ 128) are in l ^ 16.
+//   D = 512: lane l holds [8l, 8l + 8) and [256 + 8l, 256 + 8l + 8): each pair is in one lane.
+// kind: 0 = Q, 1 = K, 2 = V (weightless, not rotated). For D = 512 a K row also writes its V
+// row: the weightless norm of the same raw row with the same inverse RMS.
+template <int D>
+__device__ __forceinline__ void prep_row(const PrepArgs& a, const unsigned char* row_smem, int kind,
+                                         int lane, const float* c, const float* s,
+                                         const float* w_lo, const float* w_hi,
+                                         __nv_bfloat16* dst, __nv_bfloat16* vdst) {
+  if constexpr (D == 256) {
+    float x[8];
+    unpack8(*reinterpret_cast<const uint4*>(row_smem + lane * 16), x);
+    float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxRows256; ++i) {
-      const int row = base + i * kWarps256;
-      if (row < nrows) {
-        const __nv_bfloat16* src;
-        if (row < Hq) src = a.q_raw + (int64_t)t * a.q_stride + (int64_t)row * 256;
-        else if (row < Hq + Hkv) src = a.k_raw + (int64_t)t * a.k_stride + (int64_t)(row - Hq) * 256;
-        else src = a.v_raw + (int64_t)t * a.v_stride + (int64_t)(row - Hq - Hkv) * 256;
-        raw[i] = ld_stream(src + lane * 8);
+    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss * (1.0f / 256.0f) + a.eps);
+    float y[8];
+    if (kind == 2) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = x[e] * inv;
+    } else {
+      float u[8], pu[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) u[e] = x[e] * inv * w_lo[e];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) pu[e] = __shfl_xor_sync(0xffffffffu, u[e], 16);
+      if (lane < 16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = u[e] * c[e] - pu[e] * s[e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = u[e] * c[e] + pu[e] * s[e];
       }
     }
+    *reinterpret_cast<uint4*>(dst + lane * 8) = pack8(y);
+  } else {
+    float xa[8], xb[8];
+    unpack8(*reinterpret_cast<const uint4*>(row_smem + lane * 16), xa);
+    unpack8(*reinterpret_cast<const uint4*>(row_smem + 512 + lane * 16), xb);
+    float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxRows256; ++i) {
-      const int row = base + i * kWarps256;
-      if (row >= nrows) break;
-      float x[8];
-      unpack8(raw[i], x);
-      float ss = 0.f;
+    for (int e = 0; e < 8; ++e) ss = fmaf(xa[e], xa[e], fmaf(xb[e], xb[e], ss));
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss * (1.0f / 512.0f) + a.eps);
+    float ya[8], yb[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-      ss = warp_sum(ss);
-      const float inv = 1.0f / sqrtf(ss * (1.0f / 256.0f) + a.eps);
-      const bool is_v = row >= Hq + Hkv;
-      float y[8];
-      if (is_v) {
+    for (int e = 0; e < 8; ++e) {
+      const float ua = xa[e] * inv * w_lo[e];
+      const float ub = xb[e] * inv * w_hi[e];
+      ya[e] = ua * c[e] - ub * s[e];
+      yb[e] = ub * c[e] + ua * s[e];
+    }
+    *reinterpret_cast<uint4*>(dst + lane * 8) = pack8(ya);
+    *reinterpret_cast<uint4*>(dst + 256 + lane * 8) = pack8(yb);
+    if (kind == 1) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = x[e] * inv;
-      } else {
-        const float* w = row < Hq ? wq : wk;
-        float u[8], pu[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) u[e] = x[e] * inv * w[e];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) pu[e] = __shfl_xor_sync(0xffffffffu, u[e], 16);
-        if (half == 0) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = u[e] * c[e] - pu[e] * s[e];
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = u[e] * c[e] + pu[e] * s[e];
-        }
+      for (int e = 0; e < 8; ++e) {
+        ya[e] = xa[e] * inv;
+        yb[e] = xb[e] * inv;
       }
-      const uint4 o = pack8(y);
-      __nv_bfloat16* dst;
-      if (row < Hq) dst = a.q_out + ((int64_t)t * Hq + row) * 256;
-      else if (!is_v) dst = ts.k_row0 + (int64_t)(row - Hq) * a.pool.stride_head;
-      else dst = ts.k_row0 + a.pool.stride_kv + (int64_t)(row - Hq - Hkv) * a.pool.stride_head;
-      *reinterpret_cast<uint4*>(dst + lane * 8) = o;
+      *reinterpret_cast<uint4*>(vdst + lane * 8) = pack8(ya);
+      *reinterpret_cast<uint4*>(vdst + 256 + lane * 8) = pack8(yb);
     }
   }
 }
 
-// ----------------------------------------------------------------------------- hd512
-// Lane l holds elements [8l, 8l+8) and [256+8l, 256+8l+8): each rotary pair (i, i+256)
-// sits in one lane. Rows of a token: Hq query rows, then Hkv K rows; each K row also
-// produces its V row from the same registers and the same inverse RMS.
-constexpr int kWarps512 = 8;
-constexpr int kMaxRows512 = 2;
+// Stage layout: raw rows [Hq Q rows][Hkv K rows][Hkv V rows (D = 256 only)] of D bf16, then the
+// token's rotary row (D/2 fp32 cos, D/2 fp32 sin), then its TokMeta header; stage_bytes is a
+// multiple of 128. Shared memory: 2 * nst mbarriers and the abort flag, then the stages.
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads)
+prep_kernel(PrepArgs a, int32_t nst, uint32_t stage_bytes) {
+  extern __shared__ __align__(128) unsigned char psm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t Hq = a.num_qo_heads, Hkv = a.pool.num_kv_heads;
+  const int32_t nrows = Hq + (D == 256 ? 2 : 1) * Hkv;
+  const uint32_t rows_bytes = (uint32_t)nrows * D * 2;
+  const uint32_t hdr_off = rows_bytes + D * 4;
+  const uint32_t bars = smem_u32(psm);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(psm + 16 * nst);
+  unsigned char* stages = psm + ((16 * nst + 4 + 127) & ~127);
+  const uint32_t stages_s = smem_u32(stages);
+  auto FULL = [&](int s) { return bars + 8u * s; };
+  auto EMPTY = [&](int s) { return bars + 8u * (nst + s); };
 
-__global__ void __launch_bounds__(kWarps512 * 32)
-prep_hd512_kernel(PrepArgs a) {
-  const int32_t t = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int32_t Hq = a.num_qo_heads;
-  const int32_t Hkv = a.pool.num_kv_heads;
-  const int32_t nrows = Hq + Hkv;
-
-  TokenSlot ts;
-  if (!token_slot(a, t, &ts)) {
-    if (threadIdx.x == 0) set_status(a.status);
-    return;
+  const int32_t T = a.plan.num_tokens, G = gridDim.x;
+  const int32_t count = T > (int32_t)blockIdx.x ? (T - 1 - (int32_t)blockIdx.x) / G + 1 : 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nst; ++s) {
+      bar_init(FULL(s), 1);
+      bar_init(EMPTY(s), kPrepConsumerWarps);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  const int ci = lane * 8;
-  float c[8], s[8];
-  {
-    const float4* cp = reinterpret_cast<const float4*>(a.rope_cos + (int64_t)ts.pos * 256 + ci);
-    const float4* sp = reinterpret_cast<const float4*>(a.rope_sin + (int64_t)ts.pos * 256 + ci);
-    float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
-    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-    s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-  }
+  __syncthreads();
 
-  for (int base = warp; base < nrows; base += kWarps512 * kMaxRows512) {
-    uint4 lo[kMaxRows512], hi[kMaxRows512];
-#pragma unroll
-    for (int i = 0; i < kMaxRows512; ++i) {
-      const int row = base + i * kWarps512;
-      if (row < nrows) {
-        const __nv_bfloat16* src =
-            row < Hq ? a.q_raw + (int64_t)t * a.q_stride + (int64_t)row * 512
-                     : a.k_raw + (int64_t)t * a.k_stride + (int64_t)(row - Hq) * 512;
-        lo[i] = ld_stream(src + ci);
-        hi[i] = ld_stream(src + 256 + ci);
+  if (warp == kPrepConsumerWarps) {
+    // ---------------------------------------------------------------- producer
+    const uint32_t q_bytes = (uint32_t)Hq * D * 2, kv_bytes = (uint32_t)Hkv * D * 2;
+    const uint32_t tok_bytes = rows_bytes + D * 4;
+    bool live = true;
+    for (int32_t kb = 0; live && kb < count; kb += 32) {
+      const int n = min(32, count - kb);
+      // lane i resolves the metadata of this CTA's token kb + i
+      TokMeta m;
+      m.slot = 0;
+      m.pos = 0;
+      m.ok = 0;
+      if (lane < n && !token_meta(a, (int32_t)blockIdx.x + (kb + lane) * G, &m)) {
+        m.slot = 0;
+        m.pos = 0;
+        m.ok = 0;
+        atomicOr(a.status, kStatusBounds);
+      }
+      for (int i = 0; i < n; ++i) {
+        const int32_t k = kb + i;
+        const int st = k % nst;
+        TokMeta mi;
+        mi.slot = __shfl_sync(0xffffffffu, m.slot, i);
+        mi.pos = __shfl_sync(0xffffffffu, m.pos, i);
+        mi.ok = __shfl_sync(0xffffffffu, m.ok, i);
+        int go = 1;
+        if (lane == 0) {
+          // the consumers have released the stage's previous token
+          if (!bar_wait(EMPTY(st), ((k / nst) & 1) ^ 1, abort_flag, a.status)) {
+            go = 0;
+          } else {
+            unsigned char* sg = stages + (size_t)st * stage_bytes;
+            *reinterpret_cast<TokMeta*>(sg + hdr_off) = mi;
+            if (mi.ok) {
+              const int32_t t = (int32_t)blockIdx.x + k * G;
+              const uint32_t ss = stages_s + (uint32_t)st * stage_bytes;
+              bar_arrive_tx(FULL(st), tok_bytes);
+              bulk_g2s(ss, a.q_raw + (int64_t)t * a.q_stride, q_bytes, FULL(st));
+              bulk_g2s(ss + q_bytes, a.k_raw + (int64_t)t * a.k_stride, kv_bytes, FULL(st));
+              if (D == 256)
+                bulk_g2s(ss + q_bytes + kv_bytes, a.v_raw + (int64_t)t * a.v_stride, kv_bytes,
+                         FULL(st));
+              bulk_g2s(ss + rows_bytes, a.rope_cos + (int64_t)mi.pos * (D / 2), D * 2, FULL(st));
+              bulk_g2s(ss + rows_bytes + D * 2, a.rope_sin + (int64_t)mi.pos * (D / 2), D * 2,
+                       FULL(st));
+            } else {
+              bar_arrive(FULL(st));  // skipped token: the header says so
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, go, 0)) {
+          live = false;
+          break;
+        }
       }
     }
-#pragma unroll
-    for (int i = 0; i < kMaxRows512; ++i) {
-      const int row = base + i * kWarps512;
-      if (row >= nrows) break;
-      float xa[8], xb[8];
-      unpack8(lo[i], xa);
-      unpack8(hi[i], xb);
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(xa[e], xa[e], fmaf(xb[e], xb[e], ss));
-      ss = warp_sum(ss);
-      const float inv = 1.0f / sqrtf(ss * (1.0f / 512.0f) + a.eps);
-      const bool is_q = row < Hq;
-      const __nv_bfloat16* wp = is_q ? a.w_q : a.w_k;
-      float wa[8], wb[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(wp + ci)), wa);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(wp + 256 + ci)), wb);
-      float ya[8], yb[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float ua = xa[e] * inv * wa[e];
-        const float ub = xb[e] * inv * wb[e];
-        ya[e] = ua * c[e] - ub * s[e];
-        yb[e] = ub * c[e] + ua * s[e];
+    if (!live) {
+      // copies already issued land within microseconds; let them finish before the CTA's
+      // shared memory is released
+      const uint64_t t0 = gtimer();
+      while (gtimer() - t0 < 100000ull) {
       }
-      __nv_bfloat16* dst = is_q ? a.q_out + ((int64_t)t * Hq + row) * 512
-                                : ts.k_row0 + (int64_t)(row - Hq) * a.pool.stride_head;
-      *reinterpret_cast<uint4*>(dst + ci) = pack8(ya);
-      *reinterpret_cast<uint4*>(dst + 256 + ci) = pack8(yb);
-      if (!is_q) {
-        // V: the weightless norm of the same raw K row, same inverse RMS, no rotation.
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          ya[e] = xa[e] * inv;
-          yb[e] = xb[e] * inv;
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    // this lane's weights (Q and K), loaded once
+    float wq_lo[8], wq_hi[8], wk_lo[8], wk_hi[8];
+    {
+      const int ci = lane * 8;
+      unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_q + ci)), wq_lo);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_k + ci)), wk_lo);
+      if (D == 512) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_q + 256 + ci)), wq_hi);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_k + 256 + ci)), wk_hi);
+      }
+    }
+    // rotary column of this lane's first element
+    const int rc = D == 256 ? (lane & 15) * 8 : lane * 8;
+    for (int32_t k = 0; k < count; ++k) {
+      const int st = k % nst;
+      int okw = 1;
+      if (lane == 0) okw = bar_wait(FULL(st), (k / nst) & 1, abort_flag, a.status) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      const unsigned char* sg = stages + (size_t)st * stage_bytes;
+      const TokMeta m = *reinterpret_cast<const TokMeta*>(sg + hdr_off);
+      if (m.ok) {
+        const int32_t t = (int32_t)blockIdx.x + k * G;
+        float c[8], s[8];
+        {
+          const float4* cp = reinterpret_cast<const float4*>(sg + rows_bytes) + rc / 4;
+          const float4* sp = reinterpret_cast<const float4*>(sg + rows_bytes + D * 2) + rc / 4;
+          const float4 c0 = cp[0], c1 = cp[1], s0 = sp[0], s1 = sp[1];
+          c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+          c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+          s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+          s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
         }
-        __nv_bfloat16* vdst = dst + a.pool.stride_kv;
-        *reinterpret_cast<uint4*>(vdst + ci) = pack8(ya);
-        *reinterpret_cast<uint4*>(vdst + 256 + ci) = pack8(yb);
+        __nv_bfloat16* const kbase = a.pool.layer_base + m.slot;
+        auto do_row = [&](int row) {
+          const int kind = row < Hq ? 0 : (row < Hq + Hkv ? 1 : 2);
+          __nv_bfloat16* dst;
+          __nv_bfloat16* vdst = nullptr;
+          if (kind == 0) {
+            dst = a.q_out + ((int64_t)t * Hq + row) * D;
+          } else if (kind == 1) {
+            dst = kbase + (int64_t)(row - Hq) * a.pool.stride_head;
+            vdst = dst + a.pool.stride_kv;
+          } else {
+            dst = kbase + a.pool.stride_kv + (int64_t)(row - Hq - Hkv) * a.pool.stride_head;
+          }
+          if (kind == 0)
+            prep_row<D>(a, sg + (size_t)row * (D * 2), 0, lane, c, s, wq_lo, wq_hi, dst, vdst);
+          else
+            prep_row<D>(a, sg + (size_t)row * (D * 2), kind, lane, c, s, wk_lo, wk_hi, dst, vdst);
+        };
+        for (int row = warp; row < nrows; row += kPrepConsumerWarps) do_row(row);
       }
+      // every lane's shared-memory reads of this stage are done
+      __syncwarp();
+      if (lane == 0) bar_arrive(EMPTY(st));
     }
   }
 }
@@ -274,6 +375,54 @@ __global__ void rope_table_kernel(float* cos_t, float* sin_t, int32_t rows, int3
   }
 }
 
+// The stages of all CTAs on an SM share about 210 KB of shared memory: the CTAs an SM holds
+// (limited by registers) split it, at least two stages each, so every SM keeps ~200 KB of
+// copies in flight.
+template <int D>
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
+  const int32_t T = a.plan.num_tokens;
+  if (T <= 0) return cudaSuccess;
+  const int32_t nrows = a.num_qo_heads + (D == 256 ? 2 : 1) * a.pool.num_kv_heads;
+  const uint32_t stage = (uint32_t)((((int64_t)nrows * D * 2 + D * 4 + 16) + 127) & ~(int64_t)127);
+  // the occupancy and the attribute depend only on the device and the stage size
+  static thread_local int cached_dev = -1;
+  static thread_local uint32_t cached_stage = 0;
+  static thread_local int sms = 0, per_sm = 0, nst = 0;
+  static thread_local size_t smem = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev != cached_dev || stage != cached_stage) {
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    int by_regs = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&by_regs, prep_kernel<D>, kPrepThreads,
+                                                           0)) != cudaSuccess)
+      return e;
+    if (by_regs < 1) by_regs = 1;
+    if (by_regs > 4) by_regs = 4;
+    constexpr uint32_t kSmBudget = 210 * 1024;
+    nst = (int)(kSmBudget / by_regs / stage);
+    if (nst < 2) nst = 2;
+    if (nst > 8) nst = 8;
+    smem = (size_t)((16 * nst + 4 + 127) & ~127) + (size_t)nst * stage;
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    if ((e = cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)) != cudaSuccess)
+      return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prep_kernel<D>, kPrepThreads,
+                                                           smem)) != cudaSuccess)
+      return e;
+    if (per_sm < 1) per_sm = 1;
+    cached_dev = dev;
+    cached_stage = stage;
+  }
+  const int64_t ctas = std::min<int64_t>((int64_t)sms * per_sm, T);
+  prep_kernel<D><<<(unsigned)ctas, kPrepThreads, smem, stream>>>(a, nst, stage);
+  count_launch();
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int32_t rows, int32_t head_dim,
@@ -288,15 +437,11 @@ cudaError_t launch_rope_table(float* cos_t, float* sin_t, int32_t rows, int32_t 
 }
 
 cudaError_t launch_prep_hd256(const PrepArgs& a, cudaStream_t stream) {
-  prep_hd256_kernel<<<a.plan.num_tokens, kWarps256 * 32, 0, stream>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_prep<256>(a, stream);
 }
 
 cudaError_t launch_prep_hd512(const PrepArgs& a, cudaStream_t stream) {
-  prep_hd512_kernel<<<a.plan.num_tokens, kWarps512 * 32, 0, stream>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return launch_prep<512>(a, stream);
 }
 
 }  // namespace pg
