@@ -4,13 +4,17 @@
 // division; "feat(gemma4): paged KV serving across both attention families",
 // Description: hd256 local layers with a sliding window, hd512 global layers causal).
 //
-// One CTA owns a 128-row query tile that packs the GQA group of one KV head (rows are
-// token-major, head-minor, exactly the order a 3-D TMA box of q[token][head][d] lands
-// in shared memory) and walks the 64-key tiles of its visible key range, skipping
-// tiles outside the causal window.
+// Work unit: a 128-row query tile that packs the GQA group of one KV head (rows are
+// token-major, head-minor, exactly the order a 3-D TMA box of q[token][head][d] lands in
+// shared memory) and one 256-column part of the output; the unit walks the 64-key tiles of its
+// visible key range, skipping tiles outside the causal window. The kernel is persistent: one
+// CTA per SM (its shared and tensor memory fill the SM) takes one unit of each round of
+// gridDim.x units (longest first), so the barriers, tensor memory and K/V rings
+// carry over from unit to unit: the producers fetch the next unit's first tiles while the
+// current one finishes, and the next unit's Q enters TMEM before this unit's epilogue.
 //
 //   warp 0     K producer (TMA): one 4-D box per page (BR rows x 256 d) into a ring of
-//              three 32 KB part slots; also Q columns [256,512) once (head_dim 512)
+//              three 32 KB part slots; also each unit's Q columns [256,512) (head_dim 512)
 //   warp 10    V producer (TMA): one 3-D box per page into NVR 32 KB slots
 //   warp 1     QK issuer: S = Q K^T into a TMEM S buffer (M=128, N=64, K=16 steps; the
 //              first 256-d part reads Q from TMEM, head_dim 512's second part from shared
@@ -24,11 +28,10 @@
 //              softmax in log2 units with lazy rescaling (O is rescaled in TMEM only when a
 //              row maximum outgrows a 2^64 headroom by more than 2^48: bf16 P and fp32 O and
 //              row sums hold the range, and O / l is unchanged); then the epilogue
-//              normalises O and writes bf16 rows (full tiles staged in shared memory and
-//              written by TMA stores).
+//              normalises O and each thread stores its 256 contiguous bytes of the row.
 //
-// O holds 256 output columns: for head_dim 512 each query tile runs as two CTAs (grid z),
-// each computing the full 512-wide S and half of O. The TMEM map is described at TcCfg.
+// O holds 256 output columns: for head_dim 512 each query tile is two units, each computing
+// the full 512-wide S and half of O. The TMEM map is described at TcCfg.
 //
 // Every wait is bounded (two seconds of %globaltimer); a wait that runs out sets the
 // device status word, makes the CTA drain and free its tensor memory, and return.
@@ -38,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace pg {
@@ -77,7 +81,7 @@ struct TcCfg {
   static constexpr int P_BUF = kM * kBN * 2;          // one P buffer: 128 rows x 64 keys bf16
   static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes + (P_SMEM ? 2 * P_BUF : 0);
   static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
-  static constexpr int NBAR = 2 * NS + 21;      // ..., 4 per-producer fix-up barriers last
+  static constexpr int NBAR = 2 * NS + 22;      // ..., QFREE, 4 per-producer fix-up barriers last
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
   static constexpr int NSB = 2;                 // S buffers (and P buffers)
   static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
@@ -187,20 +191,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-// TMA store of a 3-D box from shared memory, and the bulk-group commit / wait for its reads
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, uint32_t src, int x, int y,
-                                             int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tm),
-      "r"(x), "r"(y), "r"(z), "r"(src)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -309,14 +299,44 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ kernel
+// One work unit = (query tile, KV head, 256-column part of the output). Units are numbered
+// longest first (the plan lists each request's query tiles in token order, so the last tiles
+// come first) and a persistent CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...
+struct TcUnit {
+  int32_t q0, tok0, ntok, kvp0, kvp1, kv_len, sp, kb0, ntiles, g, dh;
+};
+__device__ __forceinline__ TcUnit tc_unit(const TcArgs& a, int32_t w, int32_t ndh) {
+  const PlanDev& pl = a.plan;
+  TcUnit u;
+  const int32_t item = pl.num_work - 1 - w / (a.num_kv_heads * ndh);
+  u.g = (w / ndh) % a.num_kv_heads;
+  u.dh = w % ndh;
+  const int32_t r = pl.work_req[item];
+  u.tok0 = pl.work_tok0[item];
+  u.q0 = pl.qo_indptr[r];
+  u.ntok = min(a.cta_tile_q, pl.qo_indptr[r + 1] - u.q0 - u.tok0);
+  u.kvp0 = pl.kv_page_indptr[r];
+  u.kvp1 = pl.kv_page_indptr[r + 1];
+  u.kv_len = (u.kvp1 - u.kvp0 - 1) * a.page_size + pl.last_page_len[r];
+  u.sp = pl.start_pos[r];
+  // key range: the keys some row of this tile sees
+  const int32_t W = a.window_left;
+  const int32_t p_first = u.sp + u.tok0, p_last = p_first + u.ntok - 1;
+  const int32_t lo = W >= 0 ? max(0, p_first - W) : 0;
+  const int32_t hi = min(p_last + 1, u.kv_len);
+  u.kb0 = lo & ~(kBN - 1);
+  u.ntiles = hi > u.kb0 ? (hi - u.kb0 + kBN - 1) / kBN : 0;
+  return u;
+}
+
 template <int DQK>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-               TcArgs a) {
+               const __grid_constant__ CUtensorMap tm_v, TcArgs a) {
   using C = TcCfg<DQK>;
   constexpr int KP = C::KP, NKS = C::NKS, NVR = C::NVR, NS = C::NS;
   constexpr int NSB = C::NSB;
+  constexpr int32_t NDH = DQK / kDV;
   constexpr uint32_t kTmO = C::TM_O, kTmQ = C::TM_Q, kTmS = C::TM_S;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -330,10 +350,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   auto FULL = [&](int s) { return bars + 8u * s; };
   auto EMPTY = [&](int s) { return bars + 8u * (NS + s); };
   const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
-                 PVDONE = SFULL + 56, QFULL = SFULL + 80, EPIB = SFULL + 88,
-                 DRAIN = SFULL + 96, PAIRB = SFULL + 104;  // PAIRB: 4 barriers, one per lane quarter
-  // ring slots: K part pp of tile j is the (j KP + pp)-th part through the NKS K slots; V
-  // tile j uses V slot j mod NVR
+                 PVDONE = SFULL + 56, QFULL = SFULL + 80, DRAIN = SFULL + 96,
+                 PAIRB = SFULL + 104,  // 4 barriers, one per lane quarter
+                 QFREE = SFULL + 136;  // head_dim 512: the unit's QK MMAs have read Q's shared part
+  // ring slots, by the CTA's running tile count J: K part pp of tile J is the (J KP + pp)-th part
+  // through the NKS K slots; V tile J uses V slot J mod NVR
   auto KSLOT = [&](int32_t j, int pp) { return (int)((j * KP + pp) % NKS); };
   auto KROUND = [&](int32_t j, int pp) { return (int)((j * KP + pp) / NKS); };
   auto VSLOT = [&](int32_t j) { return NKS + (int)(j % NVR); };
@@ -343,24 +364,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PlanDev& pl = a.plan;
-  // longest work first: the plan lists each request's query tiles in token order
-  const int32_t item = pl.num_work - 1 - (int32_t)blockIdx.x;
-  const int32_t g = blockIdx.y, dh = blockIdx.z;
-  const int32_t r = pl.work_req[item], tok0 = pl.work_tok0[item];
   const int32_t G = a.group, Hq = a.num_qo_heads;
-  const int32_t q0 = pl.qo_indptr[r];
-  const int32_t ntok = min(a.cta_tile_q, pl.qo_indptr[r + 1] - q0 - tok0);
-  const int32_t kvp0 = pl.kv_page_indptr[r], kvp1 = pl.kv_page_indptr[r + 1];
   const int32_t ps = a.page_size;
-  const int32_t kv_len = (kvp1 - kvp0 - 1) * ps + pl.last_page_len[r];
-  const int32_t sp = pl.start_pos[r];
   const int32_t W = a.window_left;
-  // key range: the keys some row of this tile sees
-  const int32_t p_first = sp + tok0, p_last = sp + tok0 + ntok - 1;
-  const int32_t lo = W >= 0 ? max(0, p_first - W) : 0;
-  const int32_t hi = min(p_last + 1, kv_len);
-  const int32_t kb0 = lo & ~(kBN - 1);
-  const int32_t ntiles = hi > kb0 ? (hi - kb0 + kBN - 1) / kBN : 0;
+  const int32_t nunits = pl.num_work * a.num_kv_heads * NDH;
+  // the CTA's k-th unit: rounds of gridDim.x units, walked forwards in even rounds and
+  // backwards in odd ones, so the long and the short units of the longest-first order even out
+  auto unit_at = [&](int32_t k) -> int32_t {
+    const int32_t gs = (int32_t)gridDim.x, b = (int32_t)blockIdx.x;
+    return k * gs + ((k & 1) ? gs - 1 - b : b);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -375,12 +388,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(PFULL + 8 * b, 8);
       mbar_init(PVDONE + 8 * b, 1);
     }
-    // the eight softmax warps store Q columns [0,256) into TMEM; head_dim 512 also loads the
-    // rest by TMA
+    // per unit: the eight softmax warps store Q columns [0,256) into TMEM; head_dim 512 also
+    // loads the rest by TMA
     mbar_init(QFULL, C::QS_BYTES > 0 ? 9 : 8);
+    mbar_init(QFREE, 1);
     for (int f = 0; f < 4; ++f) mbar_init(bars + 8u * (C::NBAR - 4 + f), 1);
     mbar_init(DRAIN, 2);  // one final commit from each MMA-issuing thread
-    mbar_init(EPIB, 8);   // the softmax warps have staged their output rows
     for (int q = 0; q < 4; ++q) mbar_init(PAIRB + 8 * q, 2);
     *abort_flag = 0;
     fence_barrier_init();
@@ -401,100 +414,121 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // [key / 8][64-d chunk][8 rows][128 B] (a 4-D box), so every 8-key atom of QK's K-major
     // B operand sits 4096 bytes after the previous one across pages; V lands page-major as
     // [chunk][BR rows][128 B] (a 3-D box), which PV's MN-major B operand reads with a chunk
-    // stride of BR*128 bytes. Warp 0 also loads Q once.
+    // stride of BR*128 bytes. Warp 0 also loads Q's shared-memory part of each unit.
     const bool is_v = warp == 10;
     const uint32_t FIX = bars + 8u * (C::NBAR - 4 + (is_v ? 1 : 0));
     uint32_t fix_phase = 0;
     bool ok = true;
-    if (C::QS_BYTES > 0 && lane == 0 && warp == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
-      mbar_expect_tx(QFULL, C::QS_BYTES);
-      for (int c = 0; c < (DQK - 256) / 64; ++c)
-        tma_load_3d(sQ + c * (kM * 128), &tm_q, 256 + c * 64, g * G, q0 + tok0, QFULL);
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(is_v ? &tm_v : &tm_kv) : "memory");
+      if (C::QS_BYTES > 0 && !is_v) asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
     }
-    if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(is_v ? &tm_v : &tm_kv) : "memory");
     const int BR = a.box_rows;          // key rows per box: min(page_size, 64)
     const int nbox = kBN / BR;          // boxes (pages or page parts) per 64-key tile
     const int64_t head_rows = (int64_t)ps;
     // lane i takes box i of the tile (< nbox)
     const int my_box = lane;
     const bool box_lane = my_box < nbox;
-    auto page_of = [&](int32_t t) -> int32_t {  // raw page id of this lane's box (-1: past kv_len)
-      if (!box_lane) return -1;
-      const int32_t ks = kb0 + t * kBN + my_box * BR;
-      if (ks >= kv_len) return -1;
-      const int32_t pidx = kvp0 + ks / ps;
-      return (pidx < kvp1 && pidx < pl.num_page_ids) ? pl.page_ids[pidx] : a.num_pages;
-    };
-    auto issue_part = [&](int s, int round, int d0, int32_t t, int32_t page) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(EMPTY(s), (round & 1) ^ 1, abort_flag, a.status)))
-        return false;
-      const int32_t kb = kb0 + t * kBN;
-      const bool past = !box_lane || kb + my_box * BR >= kv_len;
-      const bool bad = !past && (page < 0 || page >= a.num_pages);
-      const bool any_bad = __any_sync(0xffffffffu, bad);
-      if (any_bad && lane == 0) atomicOr(a.status, kStatusBounds);
-      const bool load = !past && !bad;
-      // V rows past kv_len (partial last page) must read as zeros; K rows there are masked
-      const bool fix = any_bad || (is_v && __any_sync(0xffffffffu, box_lane && kb + my_box * BR + BR > kv_len));
-      const uint32_t box_bytes = (uint32_t)BR * 512u;
-      const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, load)) * box_bytes;
-      const uint32_t slot = sSlots + s * kSlotBytes;
-      const uint32_t bar = fix ? FIX : FULL(s);
-      if (lane == 0) {
-        if (bytes > 0) mbar_expect_tx(bar, bytes);
-        else if (!fix) mbar_arrive(bar);
-      }
-      __syncwarp();
-      if (load) {
-        const int32_t row = (int32_t)((((int64_t)page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + g) *
-                                          head_rows + ((kb + my_box * BR) % ps));
-        if (is_v) {
-          tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
-        } else {
-          tma_load_4d(slot + my_box * (BR * 512), &tm_kv, 0, 0, d0 / 64, row / 8, bar);
-        }
-      }
-      if (fix) {
-        if (bytes > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(FIX, fix_phase, abort_flag, a.status))) return false;
-          fix_phase ^= 1u;
-        }
-        // zero this warp's rows that must not be read: keys past kv_len, keys on bad pages
-        for (int b = 0; b < nbox; ++b) {
-          const int32_t pb = __shfl_sync(0xffffffffu, page, b);
-          for (int r = 0; r < BR; ++r) {
-            const int32_t key = kb + b * BR + r;
-            if (key < kv_len && pb >= 0 && pb < a.num_pages) continue;
-            const int c = lane >> 3, w16 = lane & 7;  // 4 chunks x 128 bytes = 32 lanes x 16 bytes
-            const int kt = b * BR + r;  // key within the tile
-            const uint32_t off = is_v ? b * (BR * 512) + c * (BR * 128) + r * 128
-                                      : (kt >> 3) * 4096 + c * 1024 + (kt & 7) * 128;
-            *(reinterpret_cast<uint4*>(gbase + (slot - base) + off) + w16) = make_uint4(0u, 0u, 0u, 0u);
+    int32_t J = 0;  // tiles of this CTA's earlier units
+    int32_t ui = 0;
+    for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
+      const TcUnit u = tc_unit(a, w, NDH);
+      if (C::QS_BYTES > 0 && !is_v) {
+        // Q columns [256,512) of this unit, once the previous unit's QK MMAs have read them
+        int go = 1;
+        if (lane == 0) {
+          if (ui > 0 && !mbar_wait(QFREE, (ui - 1) & 1, abort_flag, a.status)) {
+            go = 0;
+          } else {
+            mbar_expect_tx(QFULL, C::QS_BYTES);
+            for (int c = 0; c < (DQK - 256) / 64; ++c)
+              tma_load_3d(sQ + c * (kM * 128), &tm_q, 256 + c * 64, u.g * G, u.q0 + u.tok0, QFULL);
           }
         }
-        fence_proxy_async();
+        if (!__shfl_sync(0xffffffffu, go, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      auto page_of = [&](int32_t t) -> int32_t {  // raw page id of this lane's box (-1: past kv_len)
+        if (!box_lane) return -1;
+        const int32_t ks = u.kb0 + t * kBN + my_box * BR;
+        if (ks >= u.kv_len) return -1;
+        const int32_t pidx = u.kvp0 + ks / ps;
+        return (pidx < u.kvp1 && pidx < pl.num_page_ids) ? pl.page_ids[pidx] : a.num_pages;
+      };
+      auto issue_part = [&](int s, int round, int d0, int32_t t, int32_t page) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(EMPTY(s), (round & 1) ^ 1, abort_flag, a.status)))
+          return false;
+        const int32_t kb = u.kb0 + t * kBN;
+        const bool past = !box_lane || kb + my_box * BR >= u.kv_len;
+        const bool bad = !past && (page < 0 || page >= a.num_pages);
+        const bool any_bad = __any_sync(0xffffffffu, bad);
+        if (any_bad && lane == 0) atomicOr(a.status, kStatusBounds);
+        const bool load = !past && !bad;
+        // V rows past kv_len (partial last page) must read as zeros; K rows there are masked
+        const bool fix = any_bad || (is_v && __any_sync(0xffffffffu, box_lane && kb + my_box * BR + BR > u.kv_len));
+        const uint32_t box_bytes = (uint32_t)BR * 512u;
+        const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, load)) * box_bytes;
+        const uint32_t slot = sSlots + s * kSlotBytes;
+        const uint32_t bar = fix ? FIX : FULL(s);
+        if (lane == 0) {
+          if (bytes > 0) mbar_expect_tx(bar, bytes);
+          else if (!fix) mbar_arrive(bar);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(FULL(s));
-      }
-      return true;
-    };
-    // page ids are read two tiles ahead of the loads that use them
-    constexpr int kLook = 2;
-    int32_t qid[kLook + 1];
+        if (load) {
+          const int32_t row = (int32_t)((((int64_t)page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + u.g) *
+                                            head_rows + ((kb + my_box * BR) % ps));
+          if (is_v) {
+            tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
+          } else {
+            tma_load_4d(slot + my_box * (BR * 512), &tm_kv, 0, 0, d0 / 64, row / 8, bar);
+          }
+        }
+        if (fix) {
+          if (bytes > 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(FIX, fix_phase, abort_flag, a.status))) return false;
+            fix_phase ^= 1u;
+          }
+          // zero this warp's rows that must not be read: keys past kv_len, keys on bad pages
+          for (int b = 0; b < nbox; ++b) {
+            const int32_t pb = __shfl_sync(0xffffffffu, page, b);
+            for (int r = 0; r < BR; ++r) {
+              const int32_t key = kb + b * BR + r;
+              if (key < u.kv_len && pb >= 0 && pb < a.num_pages) continue;
+              const int c = lane >> 3, w16 = lane & 7;  // 4 chunks x 128 bytes = 32 lanes x 16 bytes
+              const int kt = b * BR + r;  // key within the tile
+              const uint32_t off = is_v ? b * (BR * 512) + c * (BR * 128) + r * 128
+                                        : (kt >> 3) * 4096 + c * 1024 + (kt & 7) * 128;
+              *(reinterpret_cast<uint4*>(gbase + (slot - base) + off) + w16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(FULL(s));
+        }
+        return true;
+      };
+      // page ids are read two tiles ahead of the loads that use them
+      constexpr int kLook = 2;
+      int32_t qid[kLook + 1];
 #pragma unroll
-    for (int i = 0; i <= kLook; ++i) qid[i] = i < ntiles ? page_of(i) : -1;
-    for (int32_t t = 0; ok && t < ntiles; ++t) {
-      const int32_t qn = t + kLook + 1 < ntiles ? page_of(t + kLook + 1) : -1;
-      if (!is_v) {
-        for (int pp = 0; ok && pp < KP; ++pp)
-          ok = issue_part(KSLOT(t, pp), KROUND(t, pp), pp * 256, t, qid[0]);
-      } else {
-        ok = issue_part(VSLOT(t), (int)(t / NVR), dh * 256, t, qid[0]);
-      }
+      for (int i = 0; i <= kLook; ++i) qid[i] = i < u.ntiles ? page_of(i) : -1;
+      for (int32_t t = 0; ok && t < u.ntiles; ++t) {
+        const int32_t qn = t + kLook + 1 < u.ntiles ? page_of(t + kLook + 1) : -1;
+        const int32_t JJ = J + t;
+        if (!is_v) {
+          for (int pp = 0; ok && pp < KP; ++pp)
+            ok = issue_part(KSLOT(JJ, pp), KROUND(JJ, pp), pp * 256, t, qid[0]);
+        } else {
+          ok = issue_part(VSLOT(JJ), (int)(JJ / NVR), u.dh * 256, t, qid[0]);
+        }
 #pragma unroll
-      for (int i = 0; i < kLook; ++i) qid[i] = qid[i + 1];
-      qid[kLook] = qn;
+        for (int i = 0; i < kLook; ++i) qid[i] = qid[i + 1];
+        qid[kLook] = qn;
+      }
+      J += u.ntiles;
     }
     if (!ok) {
       // aborting: give the copies this warp already issued time to land (they complete within
@@ -515,107 +549,115 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
     };
     bool ok = true;
-    if (warp == 1) {
-      ok = wait1(QFULL, 0);
-      for (int32_t j = 0; ok && j < ntiles; ++j) {
-        const int sb = j % NSB;
-        // S buffer sb is free once the softmax has read S(j - 2) (P_SMEM), else once PV(j - 2)
-        // has read the P stored over it
-        ok = wait1((C::P_SMEM ? SFREE : PVDONE) + 8 * sb, ((j / NSB) & 1) ^ 1);
-        if (!ok) break;
-        const uint32_t dS = tmem + kTmS + sb * kBN;
-        for (int pp = 0; ok && pp < KP; ++pp) {
-          const int sidx = KSLOT(j, pp);
-          ok = wait1(FULL(sidx), KROUND(j, pp) & 1);
+    int32_t J = 0;  // tiles of this CTA's earlier units
+    int32_t ui = 0;
+    for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
+      const int32_t ntiles = tc_unit(a, w, NDH).ntiles;
+      if (warp == 1) {
+        ok = wait1(QFULL, ui & 1);  // this unit's Q is in place
+        for (int32_t j = 0; ok && j < ntiles; ++j) {
+          const int32_t JJ = J + j;
+          const int sb = JJ % NSB;
+          // S buffer sb is free once the softmax has read S(JJ - 2) (P_SMEM), else once
+          // PV(JJ - 2) has read the P stored over it
+          ok = wait1((C::P_SMEM ? SFREE : PVDONE) + 8 * sb, ((JJ / NSB) & 1) ^ 1);
+          if (!ok) break;
+          const uint32_t dS = tmem + kTmS + sb * kBN;
+          for (int pp = 0; ok && pp < KP; ++pp) {
+            const int sidx = KSLOT(JJ, pp);
+            ok = wait1(FULL(sidx), KROUND(JJ, pp) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            // descriptors advance by 32 B per K step inside a 128-byte swizzle row and by one
+            // 64-column chunk every 4 steps: 1024 B in a K slot (8-key atoms 4096 B apart),
+            // kM x 128 B in shared-memory Q
+            const uint64_t kd0 = sdesc(sSlots + sidx * kSlotBytes, 16, 4096);
+            if (pp == 0) {
+#pragma unroll
+              for (int kk = 0; kk < 16; ++kk) {
+                const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
+                mma_ts<IDESC_QK>(dS, tmem + kTmQ + kk * 8, kd, kk > 0 ? 1u : 0u);
+              }
+            } else {
+              // an opaque copy of Q's base descriptor keeps the compiler from hoisting the 16
+              // derived descriptors out of the loop
+              uint64_t qd0 = sdesc(sQ, 16, 1024);
+              asm volatile("mov.b64 %0, %0;" : "+l"(qd0));
+#pragma unroll
+              for (int kk = 0; kk < 16; ++kk) {
+                const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
+                const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+                mma_ss<IDESC_QK>(dS, qd, kd, 1u);
+              }
+            }
+            // this part's slot is free once its MMAs (and all earlier ones) complete
+            mma_commit(EMPTY(sidx));
+          }
+          if (!ok) break;
+          mma_commit(SFULL + 8 * sb);
+        }
+        // Q's shared-memory part may be replaced once this unit's QK MMAs have completed
+        if (ok && C::QS_BYTES > 0) mma_commit(QFREE);
+      } else {
+        const int BR = a.box_rows;
+        const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 512u;
+        for (int32_t jp = 0; ok && jp < ntiles; ++jp) {
+          const int32_t JJ = J + jp;
+          const int pb = JJ % NSB;
+          const int sidx = VSLOT(JJ);
+          ok = wait1(FULL(sidx), (JJ / NVR) & 1) && wait1(PFULL + 8 * pb, (JJ / NSB) & 1);
           if (!ok) break;
           tc_fence_after();
-          // descriptors advance by 32 B per K step inside a 128-byte swizzle row and by one
-          // 64-column chunk every 4 steps: 1024 B in a K slot (8-key atoms 4096 B apart),
-          // kM x 128 B in shared-memory Q
-          const uint64_t kd0 = sdesc(sSlots + sidx * kSlotBytes, 16, 4096);
-          if (pp == 0) {
+          const uint32_t vs = sSlots + sidx * kSlotBytes;
+          // V slot: page-major boxes of BR rows, each [4 chunks][BR rows][128 B]
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-              const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
-              mma_ts<IDESC_QK>(dS, tmem + kTmQ + kk * 8, kd, kk > 0 ? 1u : 0u);
-            }
-          } else {
-            // an opaque copy of Q's base descriptor keeps the compiler from hoisting the 16
-            // derived descriptors out of the loop
-            uint64_t qd0 = sdesc(sQ, 16, 1024);
-            asm volatile("mov.b64 %0, %0;" : "+l"(qd0));
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-              const uint64_t kd = kd0 + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
-              const uint64_t qd = qd0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
-              mma_ss<IDESC_QK>(dS, qd, kd, 1u);
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint32_t key = 16u * kk;
+            const uint32_t va = vs + (key / BR) * (BR * 512u) + (key % BR) * 128u;
+            // the unit's first MMA starts O afresh
+            if constexpr (C::P_SMEM) {
+              // P buffer: K-major, 128-byte swizzled rows of 64 keys; a K step is 32 bytes
+              mma_ss<IDESC_PV>(tmem + kTmO, sdesc(sP + pb * C::P_BUF + kk * 32, 16, 1024),
+                               sdesc(va, lbo, sbo), (jp > 0 || kk > 0) ? 1u : 0u);
+            } else {
+              mma_ts<IDESC_PV>(tmem + kTmO, tmem + kTmS + pb * kBN + kk * 8, sdesc(va, lbo, sbo),
+                               (jp > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          // this part's slot is free once its MMAs (and all earlier ones) complete
           mma_commit(EMPTY(sidx));
+          mma_commit(PVDONE + 8 * pb);
         }
-        if (!ok) break;
-        mma_commit(SFULL + 8 * sb);
       }
-    } else {
-      const int BR = a.box_rows;
-      const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 512u;
-      for (int32_t jp = 0; ok && jp < ntiles; ++jp) {
-        const int pb = jp % NSB;
-        const int sidx = VSLOT(jp);
-        ok = wait1(FULL(sidx), (jp / NVR) & 1) && wait1(PFULL + 8 * pb, (jp / NSB) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vs = sSlots + sidx * kSlotBytes;
-        // V slot: page-major boxes of BR rows, each [4 chunks][BR rows][128 B]
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t key = 16u * kk;
-          const uint32_t va = vs + (key / BR) * (BR * 512u) + (key % BR) * 128u;
-          if constexpr (C::P_SMEM) {
-            // P buffer: K-major, 128-byte swizzled rows of 64 keys; a K step is 32 bytes
-            mma_ss<IDESC_PV>(tmem + kTmO, sdesc(sP + pb * C::P_BUF + kk * 32, 16, 1024),
-                             sdesc(va, lbo, sbo), (jp > 0 || kk > 0) ? 1u : 0u);
-          } else {
-            mma_ts<IDESC_PV>(tmem + kTmO, tmem + kTmS + pb * kBN + kk * 8, sdesc(va, lbo, sbo),
-                             (jp > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        mma_commit(EMPTY(sidx));
-        mma_commit(PVDONE + 8 * pb);
-      }
+      J += ntiles;
     }
     // arrives once every MMA this warp issued has completed; waited on before TMEM is freed
     mma_commit(DRAIN);
   } else if (warp >= 2 && warp <= 9) {
     // ------------------------------------------------------------ softmax + epilogue
     // Two warps per TMEM lane quarter: half h = 0 owns key columns [0,32) of each tile and
-    // output columns [0,128), half h = 1 the other halves. The row maximum of a tile is
-    // shared through shared memory; each half keeps its own partial row sum.
+    // output columns [0,128), half h = 1 the other halves. Each half keeps its own partial row
+    // sum. At the end of a unit the warps store the next unit's Q columns into TMEM (the QK
+    // MMAs of this unit are complete), so its first QK products overlap this unit's epilogue.
     const int quarter = warp & 3;
     const int h = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    const bool rvalid = row < ntok * G;
-    const int32_t prow = sp + tok0 + row / G;
-    const int32_t rlo = W >= 0 ? max(0, prow - W) : 0;
-    const int32_t rhi = min(prow + 1, kv_len);
     const uint32_t pair_bar = PAIRB + 8 * quarter;  // meeting point of the two warps sharing these rows
     uint32_t pair_phase = 0;
-    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     constexpr int HC = kBN / 2;  // key columns per half
-    {
-      // Q rows into TMEM: this thread stores its row's d columns [128h, 128h + 128) as bf16
-      // pairs (64 TMEM columns), the A operand layout of QK
+    // Q rows into TMEM: this thread stores its row's d columns [128h, 128h + 128) as bf16
+    // pairs (64 TMEM columns), the A operand layout of QK
+    auto store_q = [&](const TcUnit& v) {
+      const bool valid = row < v.ntok * G;
       const uint4* src = reinterpret_cast<const uint4*>(
-          a.q + ((int64_t)(q0 + tok0 + row / G) * Hq + g * G + row % G) * DQK + h * 128);
+          a.q + ((int64_t)(v.q0 + v.tok0 + row / G) * Hq + v.g * G + row % G) * DQK + h * 128);
       for (int half = 0; half < 2; ++half) {
         uint32_t w[32];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = rvalid ? __ldg(src + half * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        for (int q = 0; q < 8; ++q) {
+          const uint4 x = valid ? __ldg(src + half * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * q] = x.x; w[4 * q + 1] = x.y; w[4 * q + 2] = x.z; w[4 * q + 3] = x.w;
         }
         tmem_st32(tl + kTmQ + h * 64 + half * 32, w);
       }
@@ -623,179 +665,183 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(QFULL);
+    };
+    int32_t J = 0;  // tiles of this CTA's earlier units
+    TcUnit u;
+    int32_t ui = 0;
+    if (unit_at(0) < nunits) {
+      u = tc_unit(a, unit_at(0), NDH);
+      store_q(u);
     }
-    for (int32_t j = 0; ok && j < ntiles; ++j) {
-      const int b = j % NSB;
-      if (!__all_sync(0xffffffffu, mbar_wait_inline(SFULL + 8 * b, (j / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
-      tc_fence_after();
-      // both warps of the pair read the whole 64-key row: the row maximum needs no exchange
-      uint32_t sv[kBN];
-      tmem_ld32(tl + kTmS + b * kBN, sv);
-      tmem_ld32(tl + kTmS + b * kBN + 32, sv + 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      // this warp has read S(j): P_SMEM frees the S buffer for QK(j + 2); otherwise the partner
-      // warp learns that P may now overwrite it
-      if (lane == 0) mbar_arrive(C::P_SMEM ? SFREE + 8 * b : pair_bar);
-      const int32_t kb = kb0 + j * kBN;
-      const bool interior = __all_sync(0xffffffffu, rvalid && kb >= rlo && kb + kBN <= rhi);
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (interior) {
-#pragma unroll
-        for (int k = 0; k < kBN; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
-      } else {
-#pragma unroll
-        for (int k = 0; k < kBN; ++k) {
-          const int32_t key = kb + k;
-          const bool vis = rvalid && key >= rlo && key < rhi;
-          sv[k] = vis ? sv[k] : 0xFF800000u;  // -inf
-          m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
-        }
-      }
-      // scores in log2 units; a positive scale keeps the maximum where it was
-      const float raw_mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      float mx;
-      if (a.scale_log2 > 0.f) {
-        mx = raw_mx * a.scale_log2;
-      } else {
-        mx = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < kBN; ++k) mx = fmaxf(mx, __uint_as_float(sv[k]) * a.scale_log2);
-      }
-      float s[HC];
-#pragma unroll
-      for (int k = 0; k < HC; ++k) s[k] = __uint_as_float(h ? sv[HC + k] : sv[k]) * a.scale_log2;
-      float alpha = 1.f;
-      bool resc = false;
-      if (mx > m_ref + kRescaleLog2) {
-        // new reference with headroom above this maximum, so later growth rarely rescales
-        const float m_new = mx + kHeadroomLog2;
-        alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_new);
-        resc = m_ref != -INFINITY;
-        l *= alpha;
-        m_ref = m_new;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        const int jp = j - 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
+    for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
+      const int32_t ntiles = u.ntiles;
+      const bool rvalid = row < u.ntok * G;
+      const int32_t prow = u.sp + u.tok0 + row / G;
+      const int32_t rlo = W >= 0 ? max(0, prow - W) : 0;
+      const int32_t rhi = min(prow + 1, u.kv_len);
+      float m_ref = -INFINITY, l = 0.f;
+      for (int32_t j = 0; ok && j < ntiles; ++j) {
+        const int32_t JJ = J + j;
+        const int b = JJ % NSB;
+        if (!__all_sync(0xffffffffu, mbar_wait_inline(SFULL + 8 * b, (JJ / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
         tc_fence_after();
-        for (int c = 0; c < kDV / 64; ++c) {
-          uint32_t o[32];
-          const uint32_t col = kTmO + h * (kDV / 2) + c * 32;
-          tmem_ld32(tl + col, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tl + col, o);
-        }
-        tmem_wait_st();
-      }
-      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[HC / 2];
-#pragma unroll
-      for (int k = 0; k < HC / 2; ++k) {
-        // the row sum adds the bf16-rounded weights the PV product uses, so O / l is an
-        // exact weighted average of V rows (a dominant key's rounding cancels)
-        pk[k] = pack_bf16(ex2(s[2 * k] - mu), ex2(s[2 * k + 1] - mu));
-        sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
-      }
-      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      if constexpr (C::P_SMEM) {
-        // P buffer b is free once PV(j - 2) has read it
-        if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((j / NSB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
-        // this row's 32 keys: four 16-byte chunks h*4 .. h*4+3 of its 128-byte row, at
-        // positions swizzled by the row within its 8-row atom
-        unsigned char* prow = gbase + (sP - base) + b * C::P_BUF + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(prow + (((h * 4 + c) ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        fence_proxy_async();  // the PV MMA reads P through the async proxy
-        __syncwarp();
-      } else {
-        // P(j) overwrites the first half of S(j): the partner warp must have read S(j) as well
-        if (!__all_sync(0xffffffffu, mbar_wait_inline(pair_bar, pair_phase, abort_flag, a.status))) { ok = false; break; }
-        pair_phase ^= 1u;
-        tc_fence_after();
-        tmem_st16(tl + kTmS + b * kBN + h * (HC / 2), pk);
-        tmem_wait_st();
+        // both warps of the pair read the whole 64-key row: the row maximum needs no exchange
+        uint32_t sv[kBN];
+        tmem_ld32(tl + kTmS + b * kBN, sv);
+        tmem_ld32(tl + kTmS + b * kBN + 32, sv + 32);
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-      }
-      if (lane == 0) mbar_arrive(PFULL + 8 * b);
-    }
-    if (ok && ntiles > 0) {
-      const int jl = ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, abort_flag, a.status));
-    }
-    // the row sum is the sum of both halves' partial sums
-    if (ok) {
-      // swap partial row sums with the partner warp through shared memory
-      xl[h * kM + row] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pair_bar);
-      ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status));
-      if (ok) l = xl[row] + xl[kM + row];
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      if (ntok == a.cta_tile_q) {
-        // a full tile: stage the 128 x 256 output in the (now idle) ring slots as four 64-column
-        // 128-byte-swizzled boxes and write them with TMA stores
-        for (int c = 0; c < kDV / 64; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tl + kTmO + h * (kDV / 2) + c * 32, o);
-          tmem_wait_ld();
-          uint32_t w[16];
+        // this warp has read S(JJ): P_SMEM frees the S buffer for QK(JJ + 2); otherwise the
+        // partner warp learns that P may now overwrite it
+        if (lane == 0) mbar_arrive(C::P_SMEM ? SFREE + 8 * b : pair_bar);
+        const int32_t kb = u.kb0 + j * kBN;
+        const bool interior = __all_sync(0xffffffffu, rvalid && kb >= rlo && kb + kBN <= rhi);
+        if (!interior) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = ntiles == 0 ? 0u
-                               : pack_bf16(__uint_as_float(o[2 * e]) * inv,
-                                           __uint_as_float(o[2 * e + 1]) * inv);
-          const int box = h * 2 + (c >> 1), piece0 = (c & 1) * 4;
-          unsigned char* rowp = gbase + (sSlots - base) + box * (kM * 128) + row * 128;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(rowp + (((piece0 + k) ^ (row & 7)) << 4)) =
-                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-        }
-        fence_proxy_async();  // the TMA store reads the staged rows through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(EPIB);
-        if (warp == 2 && lane == 0 && mbar_wait(EPIB, 0, abort_flag, a.status)) {
-          for (int bx = 0; bx < kDV / 64; ++bx)
-            tma_store_3d(&tm_o, sSlots + bx * (kM * 128), dh * kDV + bx * 64, g * G, q0 + tok0);
-          bulk_commit();
-          bulk_wait_read();  // the staged rows must be read before the CTA's memory is released
-        }
-      } else {
-        // a partial tile (the request's last): rows past its tokens belong to the next request
-        __nv_bfloat16* dst = a.out + ((int64_t)(q0 + tok0 + row / G) * Hq + g * G + row % G) * DQK +
-                             dh * kDV + h * (kDV / 2);
-        for (int c = 0; c < kDV / 64; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tl + kTmO + h * (kDV / 2) + c * 32, o);
-          tmem_wait_ld();
-          if (ntiles == 0) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          for (int k = 0; k < kBN; ++k) {
+            const int32_t key = kb + k;
+            const bool vis = rvalid && key >= rlo && key < rhi;
+            sv[k] = vis ? sv[k] : 0xFF800000u;  // -inf
           }
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float mx;
+        float t[HC];  // this thread's 32 keys in log2 units (masked keys: -inf)
+        if (a.scale_log2 > 0.f) {
+          // a positive scale keeps the maximum where it was, and masked keys at -inf
+#pragma unroll
+          for (int k = 0; k < kBN; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+#pragma unroll
+          for (int k = 0; k < HC; ++k) t[k] = __uint_as_float(h ? sv[HC + k] : sv[k]) * a.scale_log2;
+        } else {
+#pragma unroll
+          for (int k = 0; k < kBN; ++k)
+            m4[k & 3] = fmaxf(m4[k & 3], sv[k] == 0xFF800000u ? -INFINITY : __uint_as_float(sv[k]) * a.scale_log2);
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+#pragma unroll
+          for (int k = 0; k < HC; ++k) {
+            const uint32_t v = h ? sv[HC + k] : sv[k];
+            t[k] = v == 0xFF800000u ? -INFINITY : __uint_as_float(v) * a.scale_log2;
+          }
+        }
+        float alpha = 1.f;
+        bool resc = false;
+        if (mx > m_ref + kRescaleLog2) {
+          // new reference with headroom above this maximum, so later growth rarely rescales
+          const float m_new = mx + kHeadroomLog2;
+          alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_new);
+          resc = m_ref != -INFINITY;
+          l *= alpha;
+          m_ref = m_new;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          const int32_t jp = JJ - 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
+          tc_fence_after();
+          for (int c = 0; c < kDV / 64; ++c) {
+            uint32_t o[32];
+            const uint32_t col = kTmO + h * (kDV / 2) + c * 32;
+            tmem_ld32(tl + col, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tl + col, o);
+          }
+          tmem_wait_st();
+        }
+        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[HC / 2];
+#pragma unroll
+        for (int k = 0; k < HC / 2; ++k) {
+          // the row sum adds the bf16-rounded weights the PV product uses, so O / l is an
+          // exact weighted average of V rows (a dominant key's rounding cancels)
+          pk[k] = pack_bf16(ex2(t[2 * k] - mu), ex2(t[2 * k + 1] - mu));
+          sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+        }
+        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        if constexpr (C::P_SMEM) {
+          // P buffer b is free once PV(JJ - 2) has read it
+          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ / NSB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+          // this row's 32 keys: four 16-byte chunks h*4 .. h*4+3 of its 128-byte row, at
+          // positions swizzled by the row within its 8-row atom
+          unsigned char* prow_p = gbase + (sP - base) + b * C::P_BUF + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(prow_p + (((h * 4 + c) ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          fence_proxy_async();  // the PV MMA reads P through the async proxy
+          __syncwarp();
+        } else {
+          // P(JJ) overwrites the first half of S(JJ): the partner warp must have read it as well
+          if (!__all_sync(0xffffffffu, mbar_wait_inline(pair_bar, pair_phase, abort_flag, a.status))) { ok = false; break; }
+          pair_phase ^= 1u;
+          tc_fence_after();
+          tmem_st16(tl + kTmS + b * kBN + h * (HC / 2), pk);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(PFULL + 8 * b);
+      }
+      if (!ok) break;
+      // the next unit's Q columns: this unit's QK MMAs are complete (every S was read)
+      const int32_t wn = unit_at(ui + 1);
+      TcUnit un;
+      if (wn < nunits) {
+        un = tc_unit(a, wn, NDH);
+        store_q(un);
+      }
+      if (ntiles > 0) {
+        const int32_t jl = J + ntiles - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, abort_flag, a.status));
+      }
+      // the row sum is the sum of both halves' partial sums, swapped through shared memory
+      if (ok) {
+        xl[h * kM + row] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pair_bar);
+        ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status));
+        pair_phase ^= 1u;
+        if (ok) l = xl[row] + xl[kM + row];
+        // both have read: the buffer may take the next unit's sums
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(pair_bar);
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status));
+        pair_phase ^= 1u;
+      }
+      if (ok) {
+        // epilogue: normalise this thread's 128 output columns and store them (256 contiguous
+        // bytes of the row)
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* dst = a.out + ((int64_t)(u.q0 + u.tok0 + row / G) * Hq + u.g * G + row % G) * DQK +
+                             u.dh * kDV + h * (kDV / 2);
+        for (int c = 0; c < kDV / 64; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tl + kTmO + h * (kDV / 2) + c * 32, o);
+          tmem_wait_ld();
           if (rvalid) {
-            uint32_t w[16];
+            uint32_t wv[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+              wv[e] = ntiles == 0 ? 0u
+                                  : pack_bf16(__uint_as_float(o[2 * e]) * inv,
+                                              __uint_as_float(o[2 * e + 1]) * inv);
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
-            d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+            d4[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            d4[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+            d4[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
+            d4[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
           }
         }
+        // the next unit's first PV overwrites O only after these reads
+        tc_fence_before();
       }
+      J += ntiles;
+      u = un;
     }
   }
 
@@ -839,16 +885,15 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int32_t G = a.group, TQ = a.cta_tile_q;
-  CUtensorMap tq, tkv, tv, to;
-  // Q and the output share one shape: dims (d, head, token); a box is 64 d x G heads x TQ tokens
-  for (int m = 0; m < 2; ++m) {
+  CUtensorMap tq, tkv, tv;
+  // Q: dims (d, head, token); a box is 64 d x G heads x TQ tokens
+  {
     cuuint64_t dims[3] = {(cuuint64_t)DQK, (cuuint64_t)a.num_qo_heads,
                           (cuuint64_t)a.plan.num_tokens};
     cuuint64_t strides[2] = {(cuuint64_t)DQK * 2, (cuuint64_t)a.num_qo_heads * DQK * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
     cuuint32_t es[3] = {1, 1, 1};
-    if (enc(m == 0 ? &tq : &to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-            m == 0 ? (void*)a.q : (void*)a.out, dims, strides, box, es,
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.q, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -899,20 +944,25 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   t.scale_log2 = a.sm_scale_log2;
   t.status = a.status;
 
-  static bool configured[128] = {false};
+  static int sms[128] = {0};  // the shared-memory opt-in and the SM count, per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!sms[dev]) {
     e = cudaFuncSetAttribute(attn_tc_kernel<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              TcCfg<DQK>::SMEM);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms[dev] = n > 0 ? n : 1;
   }
-  // one CTA per (query tile, KV head, 256-column half of the output)
-  const dim3 grid(a.plan.num_work, a.pool.num_kv_heads, DQK / kDV);
-  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, tv, to, t);
+  // one persistent CTA per SM (its shared and tensor memory fill the SM), each walking the
+  // units (query tile, KV head, 256-column part of the output) blockIdx.x + k * gridDim.x
+  const int64_t units = (int64_t)a.plan.num_work * a.pool.num_kv_heads * (DQK / kDV);
+  const unsigned grid = (unsigned)std::min<int64_t>(units, sms[dev]);
+  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, tv, t);
   e = cudaSuccess;
   count_launch();
   if (e != cudaSuccess) return e;
