@@ -129,19 +129,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// try_wait that lets the hardware suspend the thread until the phase completes (or kSuspendNs
-// pass) instead of spinning on the barrier word.
-constexpr uint32_t kSuspendNs = 200000;
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendNs)
-      : "memory");
-  return ok != 0;
-}
 // Bounded wait on the phase of the given parity. Returns false when the CTA is aborting
 // (another role gave up) or when this wait itself runs out of time.
 __device__ __forceinline__ bool mbar_wait_body(uint32_t bar, uint32_t parity,
@@ -149,7 +136,8 @@ __device__ __forceinline__ bool mbar_wait_body(uint32_t bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
+    // plain try_wait: with an explicit suspend-time hint, waiters woke measurably later
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       atomicOr(status, kStatusTimeout);
@@ -707,14 +695,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float mx;
-        float t[HC];  // this thread's 32 keys in log2 units (masked keys: -inf)
+        // this thread's 32 keys (masked keys: -inf); log2 units are t * tscale
+        float t[HC];
+        const float tscale = a.scale_log2 > 0.f ? a.scale_log2 : 1.f;
         if (a.scale_log2 > 0.f) {
           // a positive scale keeps the maximum where it was, and masked keys at -inf
 #pragma unroll
           for (int k = 0; k < kBN; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
           mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
 #pragma unroll
-          for (int k = 0; k < HC; ++k) t[k] = __uint_as_float(h ? sv[HC + k] : sv[k]) * a.scale_log2;
+          for (int k = 0; k < HC; ++k) t[k] = __uint_as_float(h ? sv[HC + k] : sv[k]);  // scaled below
         } else {
 #pragma unroll
           for (int k = 0; k < kBN; ++k)
@@ -758,7 +748,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int k = 0; k < HC / 2; ++k) {
           // the row sum adds the bf16-rounded weights the PV product uses, so O / l is an
           // exact weighted average of V rows (a dominant key's rounding cancels)
-          pk[k] = pack_bf16(ex2(t[2 * k] - mu), ex2(t[2 * k + 1] - mu));
+          pk[k] = pack_bf16(ex2(fmaf(t[2 * k], tscale, -mu)), ex2(fmaf(t[2 * k + 1], tscale, -mu)));
           sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
         }
         l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
