@@ -241,21 +241,23 @@ def run_reference(args):
     return 0
 
 
-def kernel_traffic(kernel_name):
-    """dram bytes per launch of a kernel from the committed ncu summary, if that capture was
-    taken on the current kernel source; otherwise None."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+def kernel_traffic(call_name):
+    """DRAM bytes per launch of a call from the committed ncu summary (profiles/traffic.md),
+    if that capture was taken on the current kernel source; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel_name)
-    if not d:
-        return None
-    src = os.path.join(ROOT, "paged_sliding_window_qkv_gb300", "csrc", d.get("source", ""))
-    if not os.path.exists(src):
-        return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != d.get("sha256"):
-        return None
-    return d.get("bytes_per_launch")
+    for line in open(p):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) < 4 or cells[0] != call_name:
+            continue
+        src = os.path.join(ROOT, "paged_sliding_window_qkv_gb300", "csrc", cells[1])
+        if not os.path.exists(src):
+            return None
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() != cells[2]:
+            return None
+        return int(cells[3])
+    return None
 
 
 def run_ours(args):
