@@ -47,10 +47,11 @@
 namespace pg {
 namespace {
 
-constexpr int kM = 128;            // query rows per CTA
+constexpr int kM = 128;            // query rows per CTA (one query tile)
 constexpr int kBN = 64;            // keys per KV tile
-constexpr int kDV = 256;           // output columns per CTA
-constexpr int kSlotBytes = kBN * 256 * 2;  // 64 keys x 256 d bf16 = 32 KB
+constexpr int kDV = 256;           // output columns per unit
+constexpr int kKH = kBN / 2;       // keys of a K tile held by each CTA of the pair
+constexpr int kSlotBytes = 16 * 1024;  // one ring slot: 32 keys x 256 d (K) or 64 keys x 128 d (V)
 constexpr int kThreadsTc = 384;  // K producer 0; QK issuer 1; softmax 2..9; V producer 10; PV issuer 11
 // Lazy rescaling: a row's reference maximum is set 2^64 above the first maximum it sees and
 // O is rescaled only when a later maximum exceeds the reference by more than 2^48. P stays
@@ -60,26 +61,29 @@ constexpr float kRescaleLog2 = 48.f;
 constexpr float kHeadroomLog2 = 64.f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// One TMEM map for both widths: O [0,256) (this CTA's 256 output columns), Q columns [0,256)
-// [256,384) (QK's first 256-d part reads A from TMEM), two S buffers [384,448) and [448,512).
-// head_dim 256 (P_SMEM): the softmax writes P(j) to one of two 16 KB shared-memory buffers
-// (PV is SS), so S(j)'s buffer is free as soon as the softmax has read it and QK(j + 2) waits
-// only for that. head_dim 512: P(j) (bf16 pairs, 32 columns) overwrites the first half of S(j)
-// once both softmax warps of a row have read it and PV(j) reads it there (TS), so QK(j + 2)
-// waits for PV(j); its shared memory instead holds Q columns [256,512) (64 KB; QK's second
-// part is SS). K streams through a ring of three 256-d part slots (a tile is KP parts; a
-// part's slot is released as soon as its 16 MMAs complete), V through NVR tile slots:
-// 6 slots for head_dim 256 (3 K + 3 V), 5 for 512 (3 + 2).
+// The kernel runs on clusters of two CTAs and issues its MMAs in the 2-SM form
+// (tcgen05 cta_group::2, M = 256): CTA c of the pair owns query tile c of a pair of adjacent
+// query tiles, its 128 rows of Q, S, P and O, and half of every K and V tile: keys
+// [32c, 32c + 32) of a K tile and output columns [128c, 128c + 128) of a V tile. The leader
+// (rank 0) issues every MMA; each product reads both CTAs' halves and writes each CTA's rows of
+// S or O into that CTA's tensor memory. Holding half a tile per CTA doubles the depth of the
+// K/V rings that the shared memory allows, which is what hides the copies' latency.
+//
+// TMEM map (each CTA, 512 columns): O [0,256) (the unit's 256 output columns), Q columns
+// [256,384) (this unit's first 256-d part of Q; QK reads A from TMEM), two S buffers
+// [384,448) and [448,512). The softmax writes P(j) to one of two 16 KB shared-memory buffers
+// (PV is SS), so QK(j + 2) waits only for both CTAs' reads of S(j). head_dim 512 also keeps Q
+// columns [256,512) in shared memory (64 KB; QK's second part is SS). K streams through NKS
+// 256-d part slots (a tile is KP parts), V through NVR tile slots.
 template <int DQK>
 struct TcCfg {
   static constexpr int KP = DQK / 256;                // K parts per tile (256 d each)
-  static constexpr int NKS = 3;                       // K part slots
-  static constexpr int NVR = DQK == 256 ? 3 : 2;      // V tile slots
+  static constexpr int NKS = DQK == 256 ? 6 : 5;      // K part slots
+  static constexpr int NVR = DQK == 256 ? 6 : 3;      // V tile slots
   static constexpr int NS = NKS + NVR;
   static constexpr int QS_BYTES = (DQK - 256) * kM * 2;  // Q columns past 256, in shared memory
-  static constexpr bool P_SMEM = DQK == 256;          // P in shared memory (else over S in TMEM)
   static constexpr int P_BUF = kM * kBN * 2;          // one P buffer: 128 rows x 64 keys bf16
-  static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes + (P_SMEM ? 2 * P_BUF : 0);
+  static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes + 2 * P_BUF;
   static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
   static constexpr int NBAR = 2 * NS + 22;      // ..., QFREE, 4 per-producer fix-up barriers last
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
@@ -95,7 +99,7 @@ struct TcArgs {
   const __nv_bfloat16* pool_layer;  // pool base of the called layer
   int64_t stride_page, stride_kv, stride_head;
   int32_t num_qo_heads, group, cta_tile_q, window_left;
-  int32_t page_size, num_pages, num_kv_heads, box_rows;
+  int32_t page_size, num_pages, num_kv_heads, box_rows_k, box_rows_v;
   float scale_log2;
   int* status;
 };
@@ -162,18 +166,53 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// ---- the CTA pair
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// arrivals on a barrier given by its cluster address (either CTA of the pair). What they
+// publish is read only by the tensor cores, from the arriving CTA's own shared or tensor memory
+// (ordered by fence.proxy.async / tcgen05 fences before the arrival), so the default release
+// (CTA scope) suffices; cluster scope measured several times slower here.
+__device__ __forceinline__ void mbar_arrive_cl(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx_cl(uint32_t cbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar), "r"(bytes)
+               : "memory");
+}
+
+// TMA loads into this CTA's shared memory whose bytes count on `bar`, a cluster address that may
+// be the leader's barrier
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
                                             int c2, int c3, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
+// L2 prefetch of a 3-D box (no shared-memory destination, no completion)
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* tm, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(tm), "r"(x),
+               "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                             int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
@@ -186,19 +225,20 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
                "r"(ncols)
                : "memory");
 }
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
-// The MMA and commit helpers below are executed by the whole issuing warp and act from lane 0
-// only. The instruction descriptor is an immediate. Measured on this kernel: with the
+// The MMA and commit helpers below are executed by the whole issuing warp of the leader CTA
+// and act from lane 0 only; the MMAs are the 2-SM form and each commit arrives on the barrier
+// at the same offset in both CTAs. The instruction descriptor is an immediate. Measured on this kernel: with the
 // descriptor in a register, or with the issuing lane picked by elect.sync, M128 MMAs issued at
 // one per ~220-290 cycles in many tiles; predicated on lane 0 with an immediate descriptor they
 // keep the tensor pipe full (32-48 cycles per M128 x N64 x K16 instruction).
@@ -206,7 +246,7 @@ template <uint32_t IDESC>
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
   asm volatile(
       "{\n .reg .pred e, p;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n setp.ne.b32 p, %3, 0;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n}\n" ::"r"(d),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %4, p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(acc), "n"(IDESC)
       : "memory");
 }
@@ -214,14 +254,15 @@ template <uint32_t IDESC>
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t acc) {
   asm volatile(
       "{\n .reg .pred e, p;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n setp.ne.b32 p, %3, 0;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n}\n" ::"r"(d),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %4, p;\n}\n" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(acc), "n"(IDESC)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "{\n .reg .pred e;\n .reg .u32 ln;\n mov.u32 ln, %%laneid;\n setp.eq.u32 e, ln, 0;\n"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}\n"
+      ::"r"(bar), "h"((uint16_t)3)
       : "memory");
 }
 
@@ -243,13 +284,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
       "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       PG_W8(0), PG_W8(8), PG_W8(16), PG_W8(24)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};" ::"r"(taddr),
-      PG_W8(0), PG_W8(8)
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
@@ -287,34 +321,44 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ kernel
-// One work unit = (query tile, KV head, 256-column part of the output). Units are numbered
-// longest first (the plan lists each request's query tiles in token order, so the last tiles
-// come first) and a persistent CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...
+// One work unit = (pair of adjacent query tiles of one request, KV head, 256-column part of the
+// output). Units are numbered longest first (the plan lists each request's tile pairs in token
+// order, so the last pairs come first); cluster i takes one unit per round of clusters.
 struct TcUnit {
-  int32_t q0, tok0, ntok, kvp0, kvp1, kv_len, sp, kb0, ntiles, g, dh;
+  int32_t q0, tok0, ntok;  // this CTA's query tile: request's first token, tile start, tokens (0: none)
+  int32_t kvp0, kvp1, kv_len, sp, kb0, ntiles, g, dh;
 };
-__device__ __forceinline__ TcUnit tc_unit(const TcArgs& a, int32_t w, int32_t ndh) {
+__device__ __forceinline__ TcUnit tc_unit(const TcArgs& a, int32_t w, int32_t ndh, int32_t rank) {
   const PlanDev& pl = a.plan;
   TcUnit u;
-  const int32_t item = pl.num_work - 1 - w / (a.num_kv_heads * ndh);
+  const int32_t pr = pl.num_pairs - 1 - w / (a.num_kv_heads * ndh);
   u.g = (w / ndh) % a.num_kv_heads;
   u.dh = w % ndh;
-  const int32_t r = pl.work_req[item];
-  u.tok0 = pl.work_tok0[item];
-  u.q0 = pl.qo_indptr[r];
-  u.ntok = min(a.cta_tile_q, pl.qo_indptr[r + 1] - u.q0 - u.tok0);
-  u.kvp0 = pl.kv_page_indptr[r];
-  u.kvp1 = pl.kv_page_indptr[r + 1];
-  u.kv_len = (u.kvp1 - u.kvp0 - 1) * a.page_size + pl.last_page_len[r];
-  u.sp = pl.start_pos[r];
-  // key range: the keys some row of this tile sees
+  // the pair's entry of the plan's pair table: two 16-byte loads, no dependent lookups
+  const int4 e0 = __ldg(reinterpret_cast<const int4*>(pl.pair_tab) + 2 * pr);
+  const int4 e1 = __ldg(reinterpret_cast<const int4*>(pl.pair_tab) + 2 * pr + 1);
+  const int32_t t0 = e0.x, len = e0.z;
+  const int32_t TQ = a.cta_tile_q;
+  u.q0 = e0.y;
+  u.sp = e0.w;
+  u.tok0 = t0 + rank * TQ;
+  u.ntok = max(0, min(TQ, len - u.tok0));
+  u.kvp0 = e1.x;
+  u.kvp1 = e1.y;
+  u.kv_len = e1.z;
+  // the pair's key range: the keys some row of either tile sees
   const int32_t W = a.window_left;
-  const int32_t p_first = u.sp + u.tok0, p_last = p_first + u.ntok - 1;
+  const int32_t p_first = u.sp + t0, p_last = u.sp + min(t0 + 2 * TQ, len) - 1;
   const int32_t lo = W >= 0 ? max(0, p_first - W) : 0;
   const int32_t hi = min(p_last + 1, u.kv_len);
   u.kb0 = lo & ~(kBN - 1);
   u.ntiles = hi > u.kb0 ? (hi - u.kb0 + kBN - 1) / kBN : 0;
   return u;
+}
+// L2 prefetch of unit w's pair-table entry, so tc_unit finds it there later
+__device__ __forceinline__ void tc_unit_prefetch(const TcArgs& a, int32_t w, int32_t ndh) {
+  const int32_t pr = a.plan.num_pairs - 1 - w / (a.num_kv_heads * ndh);
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a.plan.pair_tab + 8 * pr));
 }
 
 template <int DQK>
@@ -332,11 +376,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sSlots = base + C::QS_BYTES;
-  const uint32_t sP = sSlots + NS * kSlotBytes;  // P_SMEM: two P buffers
+  const uint32_t sP = sSlots + NS * kSlotBytes;  // two P buffers
   float* xl = reinterpret_cast<float*>(gbase + C::SMEM_DATA);  // [2 halves][128 rows]
   const uint32_t bars = base + C::SMEM_DATA + C::XL_BYTES;
   auto FULL = [&](int s) { return bars + 8u * s; };
   auto EMPTY = [&](int s) { return bars + 8u * (NS + s); };
+  // Barriers named here exist in both CTAs. FULL, SFREE, PFULL and QFULL are waited on in the
+  // leader only and count both CTAs' arrivals; EMPTY, SFULL, PVDONE, QFREE and DRAIN receive
+  // the leader's commits in both CTAs; PAIRB and the fix-up barriers are local.
   const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
                  PVDONE = SFULL + 56, QFULL = SFULL + 80, DRAIN = SFULL + 96,
                  PAIRB = SFULL + 104,  // 4 barriers, one per lane quarter
@@ -351,37 +398,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
+  const bool leader = rank == 0;
+  auto LEAD = [&](uint32_t bar) { return mapa(bar, 0); };  // the leader's copy of a barrier
   const PlanDev& pl = a.plan;
   const int32_t G = a.group, Hq = a.num_qo_heads;
   const int32_t ps = a.page_size;
   const int32_t W = a.window_left;
-  const int32_t nunits = pl.num_work * a.num_kv_heads * NDH;
-  // the CTA's k-th unit: rounds of gridDim.x units, walked forwards in even rounds and
-  // backwards in odd ones, so the long and the short units of the longest-first order even out
-  auto unit_at = [&](int32_t k) -> int32_t {
-    const int32_t gs = (int32_t)gridDim.x, b = (int32_t)blockIdx.x;
-    return k * gs + ((k & 1) ? gs - 1 - b : b);
-  };
+  const int32_t nunits = pl.num_pairs * a.num_kv_heads * NDH;
+  // the cluster's k-th unit: rounds of (number of clusters) units, walked forwards in even
+  // rounds and backwards in odd ones, so the long and the short units of the longest-first
+  // order even out
+  const int32_t ncl = (int32_t)gridDim.x / 2, ci = (int32_t)blockIdx.x / 2;
+  auto unit_at = [&](int32_t k) -> int32_t { return k * ncl + ((k & 1) ? ncl - 1 - ci : ci); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(FULL(s), 1);
+      mbar_init(FULL(s), 2);  // one arrival (with its byte count) from each CTA's producer
       mbar_init(EMPTY(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SFULL + 8 * b, 1);
-      mbar_init(SFREE + 8 * b, 8);  // P_SMEM: all softmax warps have read S
+      mbar_init(SFREE + 8 * b, 16);  // all softmax warps of both CTAs have read S
     }
     for (int b = 0; b < 3; ++b) {
-      mbar_init(PFULL + 8 * b, 8);
+      mbar_init(PFULL + 8 * b, 16);
       mbar_init(PVDONE + 8 * b, 1);
     }
-    // per unit: the eight softmax warps store Q columns [0,256) into TMEM; head_dim 512 also
-    // loads the rest by TMA
-    mbar_init(QFULL, C::QS_BYTES > 0 ? 9 : 8);
+    // per unit: the sixteen softmax warps store Q columns [0,256) into TMEM; head_dim 512 also
+    // loads the rest of each CTA's Q by TMA
+    mbar_init(QFULL, C::QS_BYTES > 0 ? 18 : 16);
     mbar_init(QFREE, 1);
     for (int f = 0; f < 4; ++f) mbar_init(bars + 8u * (C::NBAR - 4 + f), 1);
-    mbar_init(DRAIN, 2);  // one final commit from each MMA-issuing thread
+    mbar_init(DRAIN, 2);  // one final commit from each MMA-issuing warp of the leader
     for (int q = 0; q < 4; ++q) mbar_init(PAIRB + 8 * q, 2);
     *abort_flag = 0;
     fence_barrier_init();
@@ -392,45 +441,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either CTA signals the other
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == 10) {
     // ------------------------------------------------------------ producers
-    // Two warps issue the copies, one box of BR key rows x 256 d per lane: warp 0 loads K,
-    // warp 10 loads V. K lands as
+    // Each CTA loads its half of every tile: warp 0 the keys [32 rank, 32 rank + 32) of each K
+    // part, warp 10 the output columns [128 rank, 128 rank + 128) of each V tile, one box of BR
+    // key rows per lane, counted on the leader's FULL barrier. K lands as
     // [key / 8][64-d chunk][8 rows][128 B] (a 4-D box), so every 8-key atom of QK's K-major
     // B operand sits 4096 bytes after the previous one across pages; V lands page-major as
-    // [chunk][BR rows][128 B] (a 3-D box), which PV's MN-major B operand reads with a chunk
-    // stride of BR*128 bytes. Warp 0 also loads Q's shared-memory part of each unit.
+    // [chunk][BR rows][128 B] (a 3-D box of two chunks), which PV's MN-major B operand reads with
+    // a chunk stride of BR*128 bytes. Warp 0 also loads each unit's Q columns [256,512).
     const bool is_v = warp == 10;
     const uint32_t FIX = bars + 8u * (C::NBAR - 4 + (is_v ? 1 : 0));
     uint32_t fix_phase = 0;
     bool ok = true;
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(is_v ? &tm_v : &tm_kv) : "memory");
-      if (C::QS_BYTES > 0 && !is_v) asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
+      if (!is_v) asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_q) : "memory");
+      if (!is_v && unit_at(1) < nunits) tc_unit_prefetch(a, unit_at(1), NDH);
     }
-    const int BR = a.box_rows;          // key rows per box: min(page_size, 64)
-    const int nbox = kBN / BR;          // boxes (pages or page parts) per 64-key tile
+    const int BR = is_v ? a.box_rows_v : a.box_rows_k;  // key rows per box
+    const int nbox = (is_v ? kBN : kKH) / BR;            // boxes per tile half
+    const int key_off = is_v ? 0 : (int)rank * kKH;      // this CTA's first key of a tile
+    const uint32_t row_bytes = is_v ? 256u : 512u;       // bytes of one key row in a slot
     const int64_t head_rows = (int64_t)ps;
-    // lane i takes box i of the tile (< nbox)
+    // lane i takes box i of the tile half (< nbox)
     const int my_box = lane;
     const bool box_lane = my_box < nbox;
-    int32_t J = 0;  // tiles of this CTA's earlier units
+    int32_t J = 0;  // tiles of this cluster's earlier units
     int32_t ui = 0;
     for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
-      const TcUnit u = tc_unit(a, w, NDH);
+      const TcUnit u = tc_unit(a, w, NDH, (int32_t)rank);
+      if (!is_v && lane == 0) {
+        // a unit ahead, bring the next unit's pair-table entry and this CTA's Q rows of it into
+        // L2, so the softmax warps' move to that unit waits on L2 rather than DRAM
+        if (unit_at(ui + 2) < nunits) tc_unit_prefetch(a, unit_at(ui + 2), NDH);
+        if (unit_at(ui + 1) < nunits) {
+          const TcUnit un = tc_unit(a, unit_at(ui + 1), NDH, (int32_t)rank);
+          if (un.ntok > 0)
+            for (int c = 0; c < DQK / 64; ++c) tma_prefetch_3d(&tm_q, c * 64, un.g * G, un.q0 + un.tok0);
+        }
+      }
       if (C::QS_BYTES > 0 && !is_v) {
-        // Q columns [256,512) of this unit, once the previous unit's QK MMAs have read them
+        // Q columns [256,512) of this CTA's tile, once the previous unit's QK MMAs have read them
         int go = 1;
         if (lane == 0) {
           if (ui > 0 && !mbar_wait(QFREE, (ui - 1) & 1, abort_flag, a.status)) {
             go = 0;
           } else {
-            mbar_expect_tx(QFULL, C::QS_BYTES);
-            for (int c = 0; c < (DQK - 256) / 64; ++c)
-              tma_load_3d(sQ + c * (kM * 128), &tm_q, 256 + c * 64, u.g * G, u.q0 + u.tok0, QFULL);
+            mbar_expect_tx_cl(LEAD(QFULL), u.ntok > 0 ? (uint32_t)C::QS_BYTES : 0u);
+            if (u.ntok > 0)
+              for (int c = 0; c < (DQK - 256) / 64; ++c)
+                tma_load_3d(sQ + c * (kM * 128), &tm_q, 256 + c * 64, u.g * G, u.q0 + u.tok0,
+                            LEAD(QFULL));
           }
         }
         if (!__shfl_sync(0xffffffffu, go, 0)) {
@@ -440,15 +506,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       auto page_of = [&](int32_t t) -> int32_t {  // raw page id of this lane's box (-1: past kv_len)
         if (!box_lane) return -1;
-        const int32_t ks = u.kb0 + t * kBN + my_box * BR;
+        const int32_t ks = u.kb0 + t * kBN + key_off + my_box * BR;
         if (ks >= u.kv_len) return -1;
         const int32_t pidx = u.kvp0 + ks / ps;
         return (pidx < u.kvp1 && pidx < pl.num_page_ids) ? pl.page_ids[pidx] : a.num_pages;
       };
-      auto issue_part = [&](int s, int round, int d0, int32_t t, int32_t page) -> bool {
+      auto issue_part = [&](int s, int round, int c0, int32_t t, int32_t page) -> bool {
         if (!__all_sync(0xffffffffu, mbar_wait(EMPTY(s), (round & 1) ^ 1, abort_flag, a.status)))
           return false;
-        const int32_t kb = u.kb0 + t * kBN;
+        const int32_t kb = u.kb0 + t * kBN + key_off;  // first key of this CTA's half
         const bool past = !box_lane || kb + my_box * BR >= u.kv_len;
         const bool bad = !past && (page < 0 || page >= a.num_pages);
         const bool any_bad = __any_sync(0xffffffffu, bad);
@@ -456,22 +522,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const bool load = !past && !bad;
         // V rows past kv_len (partial last page) must read as zeros; K rows there are masked
         const bool fix = any_bad || (is_v && __any_sync(0xffffffffu, box_lane && kb + my_box * BR + BR > u.kv_len));
-        const uint32_t box_bytes = (uint32_t)BR * 512u;
+        const uint32_t box_bytes = (uint32_t)BR * row_bytes;
         const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, load)) * box_bytes;
         const uint32_t slot = sSlots + s * kSlotBytes;
-        const uint32_t bar = fix ? FIX : FULL(s);
+        const uint32_t bar = fix ? FIX : LEAD(FULL(s));
         if (lane == 0) {
-          if (bytes > 0) mbar_expect_tx(bar, bytes);
-          else if (!fix) mbar_arrive(bar);
+          if (!fix) mbar_expect_tx_cl(bar, bytes);
+          else if (bytes > 0) mbar_expect_tx(FIX, bytes);
         }
         __syncwarp();
         if (load) {
           const int32_t row = (int32_t)((((int64_t)page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + u.g) *
                                             head_rows + ((kb + my_box * BR) % ps));
           if (is_v) {
-            tma_load_3d(slot + my_box * (BR * 512), &tm_v, 0, row, d0 / 64, bar);
+            tma_load_3d(slot + my_box * (BR * 256), &tm_v, 0, row, c0, bar);
           } else {
-            tma_load_4d(slot + my_box * (BR * 512), &tm_kv, 0, 0, d0 / 64, row / 8, bar);
+            tma_load_4d(slot + my_box * (BR * 512), &tm_kv, 0, 0, c0, row / 8, bar);
           }
         }
         if (fix) {
@@ -485,16 +551,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int r = 0; r < BR; ++r) {
               const int32_t key = kb + b * BR + r;
               if (key < u.kv_len && pb >= 0 && pb < a.num_pages) continue;
-              const int c = lane >> 3, w16 = lane & 7;  // 4 chunks x 128 bytes = 32 lanes x 16 bytes
-              const int kt = b * BR + r;  // key within the tile
-              const uint32_t off = is_v ? b * (BR * 512) + c * (BR * 128) + r * 128
+              const int c = lane >> 3, w16 = lane & 7;  // chunk c, 16-byte piece w16 of a 128-B row
+              const int kt = b * BR + r;  // key within this CTA's half
+              if (is_v && c >= 2) continue;  // V rows are two chunks (256 B) here
+              const uint32_t off = is_v ? b * (BR * 256) + c * (BR * 128) + r * 128
                                         : (kt >> 3) * 4096 + c * 1024 + (kt & 7) * 128;
               *(reinterpret_cast<uint4*>(gbase + (slot - base) + off) + w16) = make_uint4(0u, 0u, 0u, 0u);
             }
           }
           fence_proxy_async();
           __syncwarp();
-          if (lane == 0) mbar_arrive(FULL(s));
+          if (lane == 0) mbar_arrive_cl(LEAD(FULL(s)));
         }
         return true;
       };
@@ -508,9 +575,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int32_t JJ = J + t;
         if (!is_v) {
           for (int pp = 0; ok && pp < KP; ++pp)
-            ok = issue_part(KSLOT(JJ, pp), KROUND(JJ, pp), pp * 256, t, qid[0]);
+            ok = issue_part(KSLOT(JJ, pp), KROUND(JJ, pp), pp * 4, t, qid[0]);
         } else {
-          ok = issue_part(VSLOT(JJ), (int)(JJ / NVR), u.dh * 256, t, qid[0]);
+          ok = issue_part(VSLOT(JJ), (int)(JJ / NVR), u.dh * 4 + (int)rank * 2, t, qid[0]);
         }
 #pragma unroll
         for (int i = 0; i < kLook; ++i) qid[i] = qid[i + 1];
@@ -526,29 +593,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
     }
   } else if (warp == 1 || warp == 11) {
-    // ------------------------------------------------------------ MMA issuers
-    // QK (warp 1) and PV (warp 11) are issued by two warps; they accumulate into disjoint
-    // TMEM (S and O) and are ordered against each other only through the barriers. Lane 0
-    // waits on the barriers and issues; the other lanes follow it through the loop.
-    constexpr uint32_t IDESC_QK = idesc_bf16(kM, kBN, false);
-    constexpr uint32_t IDESC_PV = idesc_bf16(kM, kDV, true);
+    // ------------------------------------------------------------ MMA issuers (the leader's)
+    // QK (warp 1) and PV (warp 11) are issued by two warps of the leader CTA; they accumulate
+    // into disjoint TMEM (S and O) of both CTAs and are ordered against each other only through
+    // the barriers. Lane 0 waits on the barriers and issues; the other lanes follow it.
+    constexpr uint32_t IDESC_QK = idesc_bf16(2 * kM, kBN, false);
+    constexpr uint32_t IDESC_PV = idesc_bf16(2 * kM, kDV, true);
     auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
       const bool r = lane == 0 ? mbar_wait_inline(bar, parity, abort_flag, a.status) : false;
       return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
     };
     bool ok = true;
-    int32_t J = 0;  // tiles of this CTA's earlier units
+    int32_t J = 0;  // tiles of this cluster's earlier units
     int32_t ui = 0;
-    for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
-      const int32_t ntiles = tc_unit(a, w, NDH).ntiles;
+    for (int32_t w = unit_at(0); leader && ok && w < nunits; w = unit_at(++ui)) {
+      const int32_t ntiles = tc_unit(a, w, NDH, 0).ntiles;
       if (warp == 1) {
-        ok = wait1(QFULL, ui & 1);  // this unit's Q is in place
+        ok = wait1(QFULL, ui & 1);  // this unit's Q is in place in both CTAs
         for (int32_t j = 0; ok && j < ntiles; ++j) {
           const int32_t JJ = J + j;
           const int sb = JJ % NSB;
-          // S buffer sb is free once the softmax has read S(JJ - 2) (P_SMEM), else once
-          // PV(JJ - 2) has read the P stored over it
-          ok = wait1((C::P_SMEM ? SFREE : PVDONE) + 8 * sb, ((JJ / NSB) & 1) ^ 1);
+          // S buffer sb is free once both CTAs' softmax warps have read S(JJ - 2)
+          ok = wait1(SFREE + 8 * sb, ((JJ / NSB) & 1) ^ 1);
           if (!ok) break;
           const uint32_t dS = tmem + kTmS + sb * kBN;
           for (int pp = 0; ok && pp < KP; ++pp) {
@@ -578,17 +644,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mma_ss<IDESC_QK>(dS, qd, kd, 1u);
               }
             }
-            // this part's slot is free once its MMAs (and all earlier ones) complete
+            // this part's slots are free once its MMAs (and all earlier ones) complete
             mma_commit(EMPTY(sidx));
           }
           if (!ok) break;
           mma_commit(SFULL + 8 * sb);
         }
-        // Q's shared-memory part may be replaced once this unit's QK MMAs have completed
+        // Q's shared-memory parts may be replaced once this unit's QK MMAs have completed
         if (ok && C::QS_BYTES > 0) mma_commit(QFREE);
       } else {
-        const int BR = a.box_rows;
-        const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 512u;
+        const int BR = a.box_rows_v;
+        const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 256u;
         for (int32_t jp = 0; ok && jp < ntiles; ++jp) {
           const int32_t JJ = J + jp;
           const int pb = JJ % NSB;
@@ -597,20 +663,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (!ok) break;
           tc_fence_after();
           const uint32_t vs = sSlots + sidx * kSlotBytes;
-          // V slot: page-major boxes of BR rows, each [4 chunks][BR rows][128 B]
+          // V slot: page-major boxes of BR rows, each [2 chunks][BR rows][128 B]
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
             const uint32_t key = 16u * kk;
-            const uint32_t va = vs + (key / BR) * (BR * 512u) + (key % BR) * 128u;
-            // the unit's first MMA starts O afresh
-            if constexpr (C::P_SMEM) {
-              // P buffer: K-major, 128-byte swizzled rows of 64 keys; a K step is 32 bytes
-              mma_ss<IDESC_PV>(tmem + kTmO, sdesc(sP + pb * C::P_BUF + kk * 32, 16, 1024),
-                               sdesc(va, lbo, sbo), (jp > 0 || kk > 0) ? 1u : 0u);
-            } else {
-              mma_ts<IDESC_PV>(tmem + kTmO, tmem + kTmS + pb * kBN + kk * 8, sdesc(va, lbo, sbo),
-                               (jp > 0 || kk > 0) ? 1u : 0u);
-            }
+            const uint32_t va = vs + (key / BR) * (BR * 256u) + (key % BR) * 128u;
+            // P buffer: K-major, 128-byte swizzled rows of 64 keys; a K step is 32 bytes. The
+            // unit's first MMA starts O afresh.
+            mma_ss<IDESC_PV>(tmem + kTmO, sdesc(sP + pb * C::P_BUF + kk * 32, 16, 1024),
+                             sdesc(va, lbo, sbo), (jp > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(EMPTY(sidx));
           mma_commit(PVDONE + 8 * pb);
@@ -618,14 +679,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       J += ntiles;
     }
-    // arrives once every MMA this warp issued has completed; waited on before TMEM is freed
-    mma_commit(DRAIN);
+    // arrives (in both CTAs) once every MMA this warp issued has completed; waited on before
+    // the pair frees its tensor memory
+    if (leader) mma_commit(DRAIN);
   } else if (warp >= 2 && warp <= 9) {
     // ------------------------------------------------------------ softmax + epilogue
     // Two warps per TMEM lane quarter: half h = 0 owns key columns [0,32) of each tile and
     // output columns [0,128), half h = 1 the other halves. Each half keeps its own partial row
     // sum. At the end of a unit the warps store the next unit's Q columns into TMEM (the QK
     // MMAs of this unit are complete), so its first QK products overlap this unit's epilogue.
+    // Arrivals that the leader's MMA warps wait on go to the leader's barriers.
     const int quarter = warp & 3;
     const int h = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
@@ -640,25 +703,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const bool valid = row < v.ntok * G;
       const uint4* src = reinterpret_cast<const uint4*>(
           a.q + ((int64_t)(v.q0 + v.tok0 + row / G) * Hq + v.g * G + row % G) * DQK + h * 128);
-      for (int half = 0; half < 2; ++half) {
-        uint32_t w[32];
+      // all sixteen loads in flight before the first store
+      uint32_t w[64];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 x = valid ? __ldg(src + half * 8 + q) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * q] = x.x; w[4 * q + 1] = x.y; w[4 * q + 2] = x.z; w[4 * q + 3] = x.w;
-        }
-        tmem_st32(tl + kTmQ + h * 64 + half * 32, w);
+      for (int q = 0; q < 16; ++q) {
+        const uint4 x = valid ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * q] = x.x; w[4 * q + 1] = x.y; w[4 * q + 2] = x.z; w[4 * q + 3] = x.w;
       }
+      tmem_st32(tl + kTmQ + h * 64, w);
+      tmem_st32(tl + kTmQ + h * 64 + 32, w + 32);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(QFULL);
+      if (lane == 0) mbar_arrive_cl(LEAD(QFULL));
     };
-    int32_t J = 0;  // tiles of this CTA's earlier units
+    int32_t J = 0;  // tiles of this cluster's earlier units
     TcUnit u;
     int32_t ui = 0;
     if (unit_at(0) < nunits) {
-      u = tc_unit(a, unit_at(0), NDH);
+      u = tc_unit(a, unit_at(0), NDH, (int32_t)rank);
       store_q(u);
     }
     for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
@@ -680,9 +743,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        // this warp has read S(JJ): P_SMEM frees the S buffer for QK(JJ + 2); otherwise the
-        // partner warp learns that P may now overwrite it
-        if (lane == 0) mbar_arrive(C::P_SMEM ? SFREE + 8 * b : pair_bar);
+        // this warp has read S(JJ): the S buffer is free for QK(JJ + 2) once all have
+        if (lane == 0) mbar_arrive_cl(LEAD(SFREE + 8 * b));
         const int32_t kb = u.kb0 + j * kBN;
         const bool interior = __all_sync(0xffffffffu, rvalid && kb >= rlo && kb + kBN <= rhi);
         if (!interior) {
@@ -752,9 +814,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
         }
         l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-        if constexpr (C::P_SMEM) {
-          // P buffer b is free once PV(JJ - 2) has read it
-          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ / NSB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+        // P buffer b is free once PV(JJ - 2) has read it
+        if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ / NSB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+        {
           // this row's 32 keys: four 16-byte chunks h*4 .. h*4+3 of its 128-byte row, at
           // positions swizzled by the row within its 8-row atom
           unsigned char* prow_p = gbase + (sP - base) + b * C::P_BUF + (row >> 3) * 1024 + (row & 7) * 128;
@@ -762,45 +824,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4*>(prow_p + (((h * 4 + c) ^ (row & 7)) << 4)) =
                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          fence_proxy_async();  // the PV MMA reads P through the async proxy
-          __syncwarp();
-        } else {
-          // P(JJ) overwrites the first half of S(JJ): the partner warp must have read it as well
-          if (!__all_sync(0xffffffffu, mbar_wait_inline(pair_bar, pair_phase, abort_flag, a.status))) { ok = false; break; }
-          pair_phase ^= 1u;
-          tc_fence_after();
-          tmem_st16(tl + kTmS + b * kBN + h * (HC / 2), pk);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
         }
-        if (lane == 0) mbar_arrive(PFULL + 8 * b);
+        fence_proxy_async();  // the PV MMA reads P through the async proxy
+        tc_fence_before();    // and after any rescaling of O in TMEM above
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cl(LEAD(PFULL + 8 * b));
       }
       if (!ok) break;
       // the next unit's Q columns: this unit's QK MMAs are complete (every S was read)
       const int32_t wn = unit_at(ui + 1);
       TcUnit un;
       if (wn < nunits) {
-        un = tc_unit(a, wn, NDH);
+        un = tc_unit(a, wn, NDH, (int32_t)rank);
         store_q(un);
       }
       if (ntiles > 0) {
         const int32_t jl = J + ntiles - 1;
         ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, abort_flag, a.status));
-      }
-      // the row sum is the sum of both halves' partial sums, swapped through shared memory
-      if (ok) {
-        xl[h * kM + row] = l;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pair_bar);
-        ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status));
-        pair_phase ^= 1u;
-        if (ok) l = xl[row] + xl[kM + row];
-        // both have read: the buffer may take the next unit's sums
-        __syncwarp();
-        if (ok && lane == 0) mbar_arrive(pair_bar);
-        ok = ok && __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status));
-        pair_phase ^= 1u;
+        // the row sum is the sum of both halves' partial sums, swapped through shared memory.
+        // The partner has read this unit's value before this warp writes the next one: that
+        // write waits for the next unit's last PV, which needs the partner's P of that tile,
+        // which it writes after this unit's epilogue.
+        if (ok) {
+          xl[h * kM + row] = l;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pair_bar);
+          ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status));
+          pair_phase ^= 1u;
+          if (ok) l = xl[row] + xl[kM + row];
+        }
       }
       if (ok) {
         // epilogue: normalise this thread's 128 output columns and store them (256 contiguous
@@ -809,22 +861,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16* dst = a.out + ((int64_t)(u.q0 + u.tok0 + row / G) * Hq + u.g * G + row % G) * DQK +
                              u.dh * kDV + h * (kDV / 2);
-        for (int c = 0; c < kDV / 64; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tl + kTmO + h * (kDV / 2) + c * 32, o);
+        for (int c2 = 0; c2 < kDV / 64; c2 += 2) {
+          // two 32-column loads in flight per wait
+          uint32_t o[64];
+          tmem_ld32(tl + kTmO + h * (kDV / 2) + c2 * 32, o);
+          tmem_ld32(tl + kTmO + h * (kDV / 2) + c2 * 32 + 32, o + 32);
           tmem_wait_ld();
           if (rvalid) {
-            uint32_t wv[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              wv[e] = ntiles == 0 ? 0u
-                                  : pack_bf16(__uint_as_float(o[2 * e]) * inv,
-                                              __uint_as_float(o[2 * e + 1]) * inv);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-            d4[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            d4[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-            d4[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
-            d4[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+            for (int c = 0; c < 2; ++c) {
+              uint32_t wv[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                wv[e] = ntiles == 0 ? 0u
+                                    : pack_bf16(__uint_as_float(o[32 * c + 2 * e]) * inv,
+                                                __uint_as_float(o[32 * c + 2 * e + 1]) * inv);
+              uint4* d4 = reinterpret_cast<uint4*>(dst + (c2 + c) * 32);
+              d4[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+              d4[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+              d4[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
+              d4[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+            }
           }
         }
         // the next unit's first PV overwrites O only after these reads
@@ -838,12 +895,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   if (warp == 1 && lane == 0) {
-    // every MMA has completed once the final commit has arrived
+    // every MMA of the pair has completed once the leader's final commits have arrived (in
+    // both CTAs)
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(DRAIN, 0) && globaltimer() - t0 < kWaitLimitNs) {
     }
   }
   __syncthreads();
+  // neither CTA frees its tensor memory or leaves while the other may still use the pair's
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -889,14 +949,15 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   const int32_t ps = a.pool.page_size;
-  const int32_t br = ps < 64 ? ps : 64;
+  const int32_t brk = ps < kKH ? ps : kKH;  // K rows per box: a page, or a CTA's 32-key half of one
+  const int32_t brv = ps < kBN ? ps : kBN;  // V rows per box
   {
-    // K: dims (64 d, row within an 8-row group, d chunk, 8-row group); one box = br rows x
+    // K: dims (64 d, row within an 8-row group, d chunk, 8-row group); one box = brk rows x
     // 256 d of one page, landing as [group][chunk][8 rows][128 B]
     const cuuint64_t rows = (cuuint64_t)a.pool.num_pages * 2 * a.pool.num_kv_heads * ps;
     cuuint64_t dims[4] = {64, 8, (cuuint64_t)DQK / 64, rows / 8};
     cuuint64_t strides[3] = {(cuuint64_t)DQK * 2, 128, (cuuint64_t)DQK * 2 * 8};
-    cuuint32_t box[4] = {64, 8, 4, (cuuint32_t)br / 8};
+    cuuint32_t box[4] = {64, 8, 4, (cuuint32_t)brk / 8};
     cuuint32_t es[4] = {1, 1, 1, 1};
     if (enc(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void*)a.pool.layer_base, dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -904,11 +965,11 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   {
-    // V: dims (64 d, row, d chunk); one box = br rows x 4 chunks (256 d) of one page
+    // V: dims (64 d, row, d chunk); one box = brv rows x 2 chunks (a CTA's 128 d) of one page
     const cuuint64_t rows = (cuuint64_t)a.pool.num_pages * 2 * a.pool.num_kv_heads * ps;
     cuuint64_t dims[3] = {64, rows, (cuuint64_t)DQK / 64};
     cuuint64_t strides[2] = {(cuuint64_t)DQK * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)br, 4};
+    cuuint32_t box[3] = {64, (cuuint32_t)brv, 2};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.pool.layer_base, dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -926,7 +987,8 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   t.page_size = ps;
   t.num_pages = a.pool.num_pages;
   t.num_kv_heads = a.pool.num_kv_heads;
-  t.box_rows = br;
+  t.box_rows_k = brk;
+  t.box_rows_v = brv;
   t.pool_layer = a.pool.layer_base;
   t.stride_page = a.pool.stride_page;
   t.stride_kv = a.pool.stride_kv;
@@ -948,14 +1010,27 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     sms[dev] = n > 0 ? n : 1;
   }
-  // one persistent CTA per SM (its shared and tensor memory fill the SM), each walking the
-  // units (query tile, KV head, 256-column part of the output) blockIdx.x + k * gridDim.x
-  const int64_t units = (int64_t)a.plan.num_work * a.pool.num_kv_heads * (DQK / kDV);
-  const unsigned grid = (unsigned)std::min<int64_t>(units, sms[dev]);
-  attn_tc_kernel<DQK><<<grid, kThreadsTc, TcCfg<DQK>::SMEM, stream>>>(tq, tkv, tv, t);
-  e = cudaSuccess;
-  count_launch();
+  // one persistent CTA per SM (its shared and tensor memory fill the SM), in clusters of two;
+  // cluster i walks the units (pair of query tiles, KV head, 256-column output part) of its
+  // rounds
+  const int64_t units = (int64_t)a.plan.num_pairs * a.pool.num_kv_heads * (DQK / kDV);
+  if (units == 0) return cudaSuccess;
+  const int64_t clusters = std::min<int64_t>(units, sms[dev] / 2 > 0 ? sms[dev] / 2 : 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(kThreadsTc, 1, 1);
+  cfg.dynamicSmemBytes = TcCfg<DQK>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<DQK>, tq, tkv, tv, t);
   if (e != cudaSuccess) return e;
+  count_launch();
   return cudaGetLastError();
 }
 

@@ -67,7 +67,7 @@ struct pg_plan {
           page_size = 0;
   int32_t max_page_id = -1, max_last_page_len = 0, max_qo_len = 0, max_kv_len = 0,
           max_pos_end = 0;
-  int32_t cta_tile_q = 0, decode = 0, kv_chunk = 0, max_chunks = 0, num_work = 0;
+  int32_t cta_tile_q = 0, decode = 0, kv_chunk = 0, max_chunks = 0, num_work = 0, num_pairs = 0;
   int32_t num_page_ids = 0;
   cudaStream_t stream = nullptr;
   int device = 0;
@@ -75,7 +75,7 @@ struct pg_plan {
   size_t dev_elems = 0;
   // offsets (elements) of each array inside `dev`
   size_t o_qo = 0, o_kvp = 0, o_pages = 0, o_last = 0, o_start = 0, o_tokreq = 0,
-         o_wreq = 0, o_wtok = 0;
+         o_wreq = 0, o_wtok = 0, o_pair = 0;
 };
 
 namespace {
@@ -137,13 +137,20 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   const int32_t cta = plan_cta_tile_q(D, group, ps);
   const int32_t chunk = plan_kv_chunk(D);
   int64_t nwork = 0;
-  std::vector<int32_t> wreq, wtok;
+  std::vector<int32_t> wreq, wtok, ptab;
   if (cta > 0) {
     for (int32_t r = 0; r < num_req; ++r) {
       const int32_t len = qo[r + 1] - qo[r];
       for (int32_t t = 0; t < len; t += cta) {
         wreq.push_back(r);
         wtok.push_back(t);
+      }
+      // the tcgen05 prefill runs query tiles in pairs (one per CTA of a cluster) that share
+      // their key tiles; a request with an odd number of tiles ends with a single-tile pair
+      for (int64_t t = 0; t < len; t += 2 * (int64_t)cta) {
+        const int32_t kv_len = (kvp[r + 1] - kvp[r] - 1) * ps + last[r];
+        const int32_t e[8] = {(int32_t)t, qo[r], len, start[r], kvp[r], kvp[r + 1], kv_len, r};
+        ptab.insert(ptab.end(), e, e + 8);
       }
     }
     nwork = (int64_t)wreq.size();
@@ -172,6 +179,7 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   q.o_tokreq = put(tokreq.data(), tokreq.size());
   q.o_wreq = put(wreq.data(), wreq.size());
   q.o_wtok = put(wtok.data(), wtok.size());
+  q.o_pair = put(ptab.data(), ptab.size());
   if (host.empty()) host.assign(4, 0);
 
   int err = PG_OK;
@@ -193,7 +201,7 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   q.max_kv_len = max_kv; q.max_pos_end = max_end;
   q.cta_tile_q = cta; q.decode = all_one ? 1 : 0; q.kv_chunk = chunk;
   q.max_chunks = max_kv > 0 ? (max_kv + chunk - 1) / chunk : 0;
-  q.num_work = (int32_t)nwork; q.num_page_ids = NP;
+  q.num_work = (int32_t)nwork; q.num_pairs = (int32_t)(ptab.size() / 8); q.num_page_ids = NP;
   q.stream = stream; q.device = dev;
   q.dev = d; q.dev_elems = host.size();
 
@@ -214,10 +222,12 @@ PlanDev plan_dev(const pg_plan* p) {
   v.tok_req = p->dev + p->o_tokreq;
   v.work_req = p->dev + p->o_wreq;
   v.work_tok0 = p->dev + p->o_wtok;
+  v.pair_tab = p->dev + p->o_pair;
   v.num_req = p->num_req;
   v.num_tokens = p->num_tokens;
   v.num_page_ids = p->num_page_ids;
   v.num_work = p->num_work;
+  v.num_pairs = p->num_pairs;
   return v;
 }
 

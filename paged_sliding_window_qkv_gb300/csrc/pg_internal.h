@@ -17,7 +17,11 @@ struct PlanDev {
   const int32_t* tok_req;         // [T]   request of each token row
   const int32_t* work_req;        // [num_work] prefill work item: request
   const int32_t* work_tok0;       // [num_work] prefill work item: first request-local token
-  int32_t num_req, num_tokens, num_page_ids, num_work;
+  // [num_pairs][8]: two consecutive query tiles of one request, with the request's geometry so
+  // a kernel reads it in one step: {first request-local token of the pair, qo_indptr[r],
+  // qo_len, start_pos, kv_page_indptr[r], kv_page_indptr[r + 1], kv_len, r}
+  const int32_t* pair_tab;
+  int32_t num_req, num_tokens, num_page_ids, num_work, num_pairs;
 };
 
 // Device view of one family's pool, already narrowed to the called layer.
