@@ -703,12 +703,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const bool valid = row < v.ntok * G;
       const uint4* src = reinterpret_cast<const uint4*>(
           a.q + ((int64_t)(v.q0 + v.tok0 + row / G) * Hq + v.g * G + row % G) * DQK + h * 128);
-      // all sixteen loads in flight before the first store
+      // all loads in flight before the first store; 32-byte loads halve the instructions, each
+      // of which touches 32 rows (one per lane)
       uint32_t w[64];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const uint4 x = valid ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
-        w[4 * q] = x.x; w[4 * q + 1] = x.y; w[4 * q + 2] = x.z; w[4 * q + 3] = x.w;
+      for (int q = 0; q < 8; ++q) {
+        if (valid) {
+          asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                       : "=r"(w[8 * q]), "=r"(w[8 * q + 1]), "=r"(w[8 * q + 2]), "=r"(w[8 * q + 3]),
+                         "=r"(w[8 * q + 4]), "=r"(w[8 * q + 5]), "=r"(w[8 * q + 6]), "=r"(w[8 * q + 7])
+                       : "l"(src + 2 * q));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[8 * q + e] = 0u;
+        }
       }
       tmem_st32(tl + kTmQ + h * 64, w);
       tmem_st32(tl + kTmQ + h * 64 + 32, w + 32);
@@ -876,11 +884,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 wv[e] = ntiles == 0 ? 0u
                                     : pack_bf16(__uint_as_float(o[32 * c + 2 * e]) * inv,
                                                 __uint_as_float(o[32 * c + 2 * e + 1]) * inv);
-              uint4* d4 = reinterpret_cast<uint4*>(dst + (c2 + c) * 32);
-              d4[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-              d4[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-              d4[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
-              d4[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+              // 32-byte stores: each instruction touches 32 rows (one per lane)
+              __nv_bfloat16* d = dst + (c2 + c) * 32;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh)
+                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d + 16 * hh),
+                             "r"(wv[8 * hh]), "r"(wv[8 * hh + 1]), "r"(wv[8 * hh + 2]), "r"(wv[8 * hh + 3]),
+                             "r"(wv[8 * hh + 4]), "r"(wv[8 * hh + 5]), "r"(wv[8 * hh + 6]), "r"(wv[8 * hh + 7])
+                             : "memory");
             }
           }
         }
