@@ -161,26 +161,31 @@ attn_split_kernel(AttnArgs a) {
     }
   }
   const __nv_bfloat16* kv_base = a.pool.layer_base + (int64_t)g * a.pool.stride_head;
+  // each thread copies the chunks c0, c0 + TPK, ... of one key row: one page lookup per row,
+  // and the TPK threads of a row move consecutive 16-byte chunks
+  constexpr int TPK = kThreads / BN;  // threads per key row
+  static_assert(kThreads % BN == 0 && C::CH % TPK == 0, "key-row copy split");
   auto load_kv = [&](int stage, int32_t kb) {
     const uint32_t bk = smem_u32(sK + stage * C::KV_BYTES);
     const uint32_t bv = smem_u32(sV + stage * C::KV_BYTES);
-    for (int idx = tid; idx < BN * C::CH; idx += kThreads) {
-      const int jj = idx / C::CH, c = idx % C::CH;
-      const int32_t j = kb + jj;
-      bool valid = j < hi;
-      const __nv_bfloat16* src = a.pool.layer_base;
-      if (valid) {
-        const int32_t pidx = kvp0 + j / ps;
-        const int32_t page = pidx < kvp1 ? pl.page_ids[pidx] : -1;
-        if (page < 0 || page >= a.pool.num_pages) {
-          if (c == 0) atomicOr(a.status, kStatusBounds);
-          valid = false;
-        } else {
-          src = kv_base + (int64_t)page * a.pool.stride_page + (int64_t)(j % ps) * D + c * 8;
-        }
+    const int jj = tid / TPK, c0 = tid % TPK;
+    const int32_t j = kb + jj;
+    bool valid = j < hi;
+    const __nv_bfloat16* src = a.pool.layer_base;
+    if (valid) {
+      const int32_t pidx = kvp0 + j / ps;
+      const int32_t page = pidx < kvp1 ? pl.page_ids[pidx] : -1;
+      if (page < 0 || page >= a.pool.num_pages) {
+        if (c0 == 0) atomicOr(a.status, kStatusBounds);
+        valid = false;
+      } else {
+        src = kv_base + (int64_t)page * a.pool.stride_page + (int64_t)(j % ps) * D;
       }
-      cp_async16(bk + swz<D>(jj, c), src, valid);
-      cp_async16(bv + swz<D>(jj, c), src + (valid ? a.pool.stride_kv : 0), valid);
+    }
+#pragma unroll
+    for (int c = c0; c < C::CH; c += TPK) {
+      cp_async16(bk + swz<D>(jj, c), src + (valid ? c * 8 : 0), valid);
+      cp_async16(bv + swz<D>(jj, c), src + (valid ? a.pool.stride_kv + c * 8 : 0), valid);
     }
   };
 
@@ -417,10 +422,10 @@ attn_merge_kernel(AttnArgs a) {
 
 using Pre256 = Cfg<256, 64, 32, 2, 1, false>;
 using Pre512 = Cfg<512, 32, 32, 1, 1, false>;
-// decode: deeper stage rings (Cfg's NS) measured no faster; the per-tile chain of the CTA,
-// not the loads in flight, bounds these shapes
-using Dec256 = Cfg<256, 16, 32, 1, 2, true>;
-using Dec512 = Cfg<512, 16, 32, 1, 2, true>;
+// decode streams K/V from HBM: three stages keep two tiles of loads in flight behind the one
+// being computed
+using Dec256 = Cfg<256, 16, 32, 1, 2, true, 3>;
+using Dec512 = Cfg<512, 16, 32, 1, 2, true, 3>;
 
 template <class C>
 cudaError_t launch_split(const AttnArgs& a, dim3 grid, cudaStream_t stream) {
