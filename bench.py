@@ -365,32 +365,62 @@ def run_ours(args):
     roof["traffic"] = kernel_traffic(dom_name)
 
     # ---- end to end through the public API with host buffers ----
-    pinned_in, pinned_out, dev_in = [], [], []
+    # Each call's inputs are copied in from pinned host memory on a copy stream and its output
+    # copied back on another, so the copies of one call overlap the kernels of its neighbours
+    # (a serving loop pipelines them the same way); the timed region runs from the first
+    # host-to-device copy to the last device-to-host copy.
+    inputs, outputs = [], []
     h2d = d2h = 0
     for _, r in runs:
+        pairs = []
         for t in [r.q_raw, r.k_raw, r.v_raw]:
             if t is None:
                 continue
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
             h.copy_(t)
-            pinned_in.append(h)
-            dev_in.append(t)
+            pairs.append((h, t))
             h2d += t.numel() * t.element_size()
+        inputs.append(pairs)
         o = torch.empty(r.out.shape, dtype=r.out.dtype, pin_memory=True)
-        pinned_out.append((o, r.out))
+        outputs.append((o, r.out))
         d2h += r.out.numel() * r.out.element_size()
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def e2e_step():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h2d_stream.wait_event(e0)
+        landed = []
+        for pairs in inputs:
+            with torch.cuda.stream(h2d_stream):
+                for h, d in pairs:
+                    d.copy_(h, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(h2d_stream)
+            landed.append(ev)
+        for i, (name, r) in enumerate(runs):
+            stream.wait_event(landed[i])
+            pg.check(r.prep_status(), name + " prep")
+            pg.check(r.attn_status(), name + " attention")
+            done = torch.cuda.Event()
+            done.record(stream)
+            d2h_stream.wait_event(done)
+            with torch.cuda.stream(d2h_stream):
+                outputs[i][0].copy_(outputs[i][1], non_blocking=True)
+        back = torch.cuda.Event()
+        back.record(d2h_stream)
+        stream.wait_event(back)
+        e1.record(stream)
+        return e0, e1
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
     e2e_ms = []
     for k in range(args.steps):
         flush.zero_()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for h, d in zip(pinned_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in pinned_out:
-            h.copy_(d, non_blocking=True)
-        e1.record(stream)
+        e0, e1 = e2e_step()
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
     t_e2e = float(np.mean(e2e_ms))
