@@ -9,8 +9,8 @@
 // bytes on the stage's mbarrier), several tokens ahead, so every SM keeps hundreds of KB of
 // loads in flight without holding them in registers. Eight consumer warps each own whole
 // head rows of the staged token: a lane reads 16-byte vectors from shared memory (a 256-wide
-// row is one conflict-free 512-byte read per warp), the RMS reduction is a warp shuffle, the
-// hd256 rotary partner lives in lane ^ 16 and the hd512 partner in the same lane, and every
+// row is one conflict-free 512-byte read per warp), the RMS reduction is a warp shuffle, each
+// lane holds both elements of its rotary pairs, and every
 // result row is one coalesced 512-byte (or 1 KB) store: q_out rows, or K/V rows at the
 // token's paged slot. The producer also resolves each token's request, position and page
 // (32 tokens at a time, one per lane) and passes them to the consumers in the stage header.
@@ -136,9 +136,10 @@ __device__ __forceinline__ bool token_meta(const PrepArgs& a, int32_t t, TokMeta
   return true;
 }
 
-// Normalise (and for Q/K rows weight and rotate) one staged row and store it.
-//   D = 256: lane l holds elements [8l, 8l + 8); its rotary partners (i -/+ 128) are in l ^ 16.
-//   D = 512: lane l holds [8l, 8l + 8) and [256 + 8l, 256 + 8l + 8): each pair is in one lane.
+// Normalise (and for Q/K rows weight and rotate) one staged row and store it. Each rotary pair
+// (i, i + D/2) sits in one lane, so the rotation needs no shuffle:
+//   D = 256: lane l holds elements [4l, 4l + 4) and [128 + 4l, 128 + 4l + 4);
+//   D = 512: lane l holds [8l, 8l + 8) and [256 + 8l, 256 + 8l + 8).
 // kind: 0 = Q, 1 = K, 2 = V (weightless, not rotated). For D = 512 a K row also writes its V
 // row: the weightless norm of the same raw row with the same inverse RMS.
 template <int D>
@@ -147,32 +148,46 @@ __device__ __forceinline__ void prep_row(const PrepArgs& a, const unsigned char*
                                          const float* w_lo, const float* w_hi,
                                          __nv_bfloat16* dst, __nv_bfloat16* vdst) {
   if constexpr (D == 256) {
-    float x[8];
-    unpack8(*reinterpret_cast<const uint4*>(row_smem + lane * 16), x);
+    // lane l: elements [4l, 4l + 4) and their rotary partners [128 + 4l, 128 + 4l + 4)
+    float xa[4], xb[4];
+    {
+      const uint2 va = *reinterpret_cast<const uint2*>(row_smem + lane * 8);
+      const uint2 vb = *reinterpret_cast<const uint2*>(row_smem + 256 + lane * 8);
+      xa[0] = __uint_as_float(va.x << 16); xa[1] = __uint_as_float(va.x & 0xFFFF0000u);
+      xa[2] = __uint_as_float(va.y << 16); xa[3] = __uint_as_float(va.y & 0xFFFF0000u);
+      xb[0] = __uint_as_float(vb.x << 16); xb[1] = __uint_as_float(vb.x & 0xFFFF0000u);
+      xb[2] = __uint_as_float(vb.y << 16); xb[3] = __uint_as_float(vb.y & 0xFFFF0000u);
+    }
     float ss = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+    for (int e = 0; e < 4; ++e) ss = fmaf(xa[e], xa[e], fmaf(xb[e], xb[e], ss));
     ss = warp_sum(ss);
     const float inv = 1.0f / sqrtf(ss * (1.0f / 256.0f) + a.eps);
-    float y[8];
+    float ya[4], yb[4];
     if (kind == 2) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = x[e] * inv;
+      for (int e = 0; e < 4; ++e) {
+        ya[e] = xa[e] * inv;
+        yb[e] = xb[e] * inv;
+      }
     } else {
-      float u[8], pu[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) u[e] = x[e] * inv * w_lo[e];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) pu[e] = __shfl_xor_sync(0xffffffffu, u[e], 16);
-      if (lane < 16) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = u[e] * c[e] - pu[e] * s[e];
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = u[e] * c[e] + pu[e] * s[e];
+      for (int e = 0; e < 4; ++e) {
+        const float ua = xa[e] * inv * w_lo[e];
+        const float ub = xb[e] * inv * w_hi[e];
+        ya[e] = ua * c[e] - ub * s[e];
+        yb[e] = ub * c[e] + ua * s[e];
       }
     }
-    *reinterpret_cast<uint4*>(dst + lane * 8) = pack8(y);
+    uint2 oa, ob;
+    {
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(ya[0], ya[1]), h1 = __floats2bfloat162_rn(ya[2], ya[3]);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(yb[0], yb[1]), h3 = __floats2bfloat162_rn(yb[2], yb[3]);
+      oa = make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
+      ob = make_uint2(*reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+    }
+    *reinterpret_cast<uint2*>(dst + lane * 4) = oa;
+    *reinterpret_cast<uint2*>(dst + 128 + lane * 4) = ob;
   } else {
     float xa[8], xb[8];
     unpack8(*reinterpret_cast<const uint4*>(row_smem + lane * 16), xa);
@@ -302,17 +317,25 @@ prep_kernel(PrepArgs a, int32_t nst, uint32_t stage_bytes) {
     // ---------------------------------------------------------------- consumers
     // this lane's weights (Q and K), loaded once
     float wq_lo[8], wq_hi[8], wk_lo[8], wk_hi[8];
-    {
+    if (D == 512) {
       const int ci = lane * 8;
       unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_q + ci)), wq_lo);
       unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_k + ci)), wk_lo);
-      if (D == 512) {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_q + 256 + ci)), wq_hi);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_k + 256 + ci)), wk_hi);
-      }
+      unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_q + 256 + ci)), wq_hi);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_k + 256 + ci)), wk_hi);
+    } else {
+      const int ci = lane * 4;
+      auto un4 = [](uint2 v, float* f) {
+        f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+      };
+      un4(__ldg(reinterpret_cast<const uint2*>(a.w_q + ci)), wq_lo);
+      un4(__ldg(reinterpret_cast<const uint2*>(a.w_k + ci)), wk_lo);
+      un4(__ldg(reinterpret_cast<const uint2*>(a.w_q + 128 + ci)), wq_hi);
+      un4(__ldg(reinterpret_cast<const uint2*>(a.w_k + 128 + ci)), wk_hi);
     }
     // rotary column of this lane's first element
-    const int rc = D == 256 ? (lane & 15) * 8 : lane * 8;
+    const int rc = D == 256 ? lane * 4 : lane * 8;
     for (int32_t k = 0; k < count; ++k) {
       const int st = k % nst;
       int okw = 1;
@@ -326,7 +349,8 @@ prep_kernel(PrepArgs a, int32_t nst, uint32_t stage_bytes) {
         {
           const float4* cp = reinterpret_cast<const float4*>(sg + rows_bytes) + rc / 4;
           const float4* sp = reinterpret_cast<const float4*>(sg + rows_bytes + D * 2) + rc / 4;
-          const float4 c0 = cp[0], c1 = cp[1], s0 = sp[0], s1 = sp[1];
+          // D = 256 uses c[0..4), s[0..4) only
+          const float4 c0 = cp[0], c1 = D == 512 ? cp[1] : c0, s0 = sp[0], s1 = D == 512 ? sp[1] : s0;
           c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
           c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
           s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
