@@ -1,0 +1,101 @@
+/*
+ * pg_kv.h -- host-side page accounting for two-family paged KV serving.
+ *
+ * Source: "feat(gemma4): paged KV serving across both attention families", Description: one
+ * pool per attention family (hd256 local layers with a sliding window, hd512 global layers),
+ * a per-request state in each, admission that is atomic across both pools with the page
+ * count as the exact frontier account, nothing changing state before a step is admissible,
+ * page ids meaningful only against the pool that issued them, and the path failing closed
+ * at the sliding window (cache slots equal positions only below it). Verification: a forced
+ * partial failure leaves both pools at their pre-request occupancy.
+ *
+ * This is host code only (no CUDA calls, no device memory). A server owns two page
+ * allocators, one per family; each request holds a state in both: its page list and its
+ * frontier (the number of KV positions written, the same in both families). The page lists
+ * feed pg_plan_paged_prefill's kv_page_indptr / page_ids / last_page_len / start_pos.
+ *
+ * Errors: int status, PG_KV_OK = 0, negative = error. On any error no state changes: both
+ * pools keep their occupancy and every request keeps its pages and frontier.
+ * Not thread-safe: one server is driven by one thread (the serving loop's step boundary).
+ */
+#ifndef PG_KV_H_
+#define PG_KV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pg_kv_server* pg_kv_server_t;  /* opaque; owns both pools' allocators */
+
+enum {
+  PG_KV_OK = 0,
+  PG_KV_ERR_ARG = -101,       /* null pointer, non-positive size, unknown family            */
+  PG_KV_ERR_NO_PAGES = -102,  /* a family's pool cannot cover the step (admission refused)   */
+  PG_KV_ERR_WINDOW = -103,    /* the step would carry the local family past its window      */
+  PG_KV_ERR_ROPE = -104,      /* the step's last position is at or past the rotary tables   */
+  PG_KV_ERR_FOREIGN = -105,   /* the request id was not issued by this server, or is closed  */
+  PG_KV_ERR_FRONTIER = -106,  /* a request's families disagree on the frontier, or a family
+                                 holds other than the pages its frontier accounts for        */
+  PG_KV_ERR_CAPACITY = -107   /* a caller buffer is too small                                */
+};
+
+enum { PG_KV_LOCAL = 0, PG_KV_GLOBAL = 1 };  /* the two families: hd256 local, hd512 global */
+
+/* Create a server with `pages_local` / `pages_global` pages of `page_size` slots in the two
+ * pools. window_left (>= 0, the local family's inclusive window) and fail_closed_at_window: when
+ * nonzero, a step whose KV length would exceed window_left + 1 positions is refused
+ * (PG_KV_ERR_WINDOW), because beyond the window cache slots would have to stop equalling
+ * positions. rope_rows: positions must stay below it. Pages are issued lowest id first. */
+int pg_kv_server_create(pg_kv_server_t* out, int32_t pages_local, int32_t pages_global,
+                        int32_t page_size, int32_t window_left, int32_t fail_closed_at_window,
+                        int32_t rope_rows);
+void pg_kv_server_destroy(pg_kv_server_t srv);
+
+/* Open a request (frontier 0, no pages) and return its id (> 0, never reused by this server). */
+int pg_kv_request_open(pg_kv_server_t srv, int64_t* request_id);
+
+/* Close a request: its pages return to both pools. PG_KV_ERR_FOREIGN for an unknown id. */
+int pg_kv_request_close(pg_kv_server_t srv, int64_t request_id);
+
+/* Admit one step of `n_tokens` (>= 1) new positions for a request, in both families at once.
+ * The page count per family is the exact frontier account: ceil((frontier + n_tokens) /
+ * page_size) minus the pages the family already holds. Before anything changes, the request
+ * must belong to this server, both families must sit at the same frontier and hold exactly the
+ * pages it accounts for, and the window and rotary bounds must hold. Then both families'
+ * pages are reserved; if either pool refuses, the other reservation is dropped and
+ * PG_KV_ERR_NO_PAGES returned, with both pools at their pre-request occupancy. Only when both
+ * reservations stand are they committed and the frontier advanced. */
+int pg_kv_admit_step(pg_kv_server_t srv, int64_t request_id, int32_t n_tokens);
+
+/* A request's frontier (positions written) and, per family, its page count. */
+int pg_kv_request_info(pg_kv_server_t srv, int64_t request_id, int32_t* frontier,
+                       int32_t* pages_local, int32_t* pages_global);
+
+/* Copy a request's page ids in one family (in position order) into out[0, cap);
+ * *n receives the count. PG_KV_ERR_CAPACITY if cap is too small (nothing written). */
+int pg_kv_request_pages(pg_kv_server_t srv, int64_t request_id, int32_t family, int32_t* out,
+                        int32_t cap, int32_t* n);
+
+/* Free pages in a family's pool. */
+int pg_kv_free_pages(pg_kv_server_t srv, int32_t family, int32_t* n);
+
+/* Test hook (the forced partial failure of the pages' verification): the next `count`
+ * reservations in `family` are refused as if that pool were full. */
+int pg_kv_inject_refusal(pg_kv_server_t srv, int32_t family, int32_t count);
+
+/* Plan inputs of a batch for one family, after each request's admitted step of step_tokens[i]
+ * tokens: kv_page_indptr [n + 1], page_ids (cap entries), last_page_len [n], start_pos [n]
+ * (= frontier - step_tokens[i]), in the layout pg_plan_paged_prefill reads. Each step must be
+ * no longer than the request's frontier. *n_page_ids receives the page-id count. */
+int pg_kv_batch_plan_inputs(pg_kv_server_t srv, int32_t family, int32_t n,
+                            const int64_t* request_ids, const int32_t* step_tokens,
+                            int64_t* kv_page_indptr, int32_t* page_ids, int32_t cap,
+                            int32_t* last_page_len, int64_t* start_pos, int32_t* n_page_ids);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* PG_KV_H_ */

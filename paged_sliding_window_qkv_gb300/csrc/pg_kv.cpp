@@ -1,0 +1,199 @@
+// Host-side page accounting for two-family paged KV serving ("feat(gemma4): paged KV serving
+// across both attention families", Description and Verification): one page allocator per
+// family, a per-request state in both, admission atomic across both pools with the page count
+// as the exact frontier account, every check before any state changes, and the local family
+// failing closed at its sliding window. Declared in include/pg_kv.h.
+#include "../../include/pg_kv.h"
+
+#include <cstdint>
+#include <new>
+#include <set>
+#include <unordered_map>
+#include <vector>
+
+namespace {
+
+struct KvRequest {
+  int32_t frontier[2] = {0, 0};     // positions written, per family (kept equal)
+  std::vector<int32_t> pages[2];    // page ids in position order, per family
+};
+
+int32_t pages_for(int64_t len, int32_t ps) { return (int32_t)((len + ps - 1) / ps); }
+
+}  // namespace
+
+struct pg_kv_server {
+  int32_t page_size = 0, window_left = 0, fail_closed = 0, rope_rows = 0;
+  std::set<int32_t> free_pages[2];  // lowest id first
+  int32_t refusals[2] = {0, 0};     // injected refusals still to come
+  int64_t next_id = 1;
+  std::unordered_map<int64_t, KvRequest> requests;
+
+  // Take `need` pages from a family's pool, or none (false) when the pool cannot cover them
+  // or a refusal was injected.
+  bool reserve(int family, int32_t need, std::vector<int32_t>* got) {
+    got->clear();
+    if (need <= 0) return true;
+    if (refusals[family] > 0) {
+      --refusals[family];
+      return false;
+    }
+    if ((int64_t)free_pages[family].size() < need) return false;
+    auto it = free_pages[family].begin();
+    for (int32_t i = 0; i < need; ++i) got->push_back(*it++);
+    free_pages[family].erase(free_pages[family].begin(), it);
+    return true;
+  }
+  void give_back(int family, const std::vector<int32_t>& pages) {
+    free_pages[family].insert(pages.begin(), pages.end());
+  }
+  // The frontier account: both families at one frontier, each holding exactly its pages.
+  bool consistent(const KvRequest& r) const {
+    if (r.frontier[0] != r.frontier[1]) return false;
+    for (int f = 0; f < 2; ++f)
+      if ((int64_t)r.pages[f].size() != pages_for(r.frontier[f], page_size)) return false;
+    return true;
+  }
+};
+
+extern "C" {
+
+int pg_kv_server_create(pg_kv_server_t* out, int32_t pages_local, int32_t pages_global,
+                        int32_t page_size, int32_t window_left, int32_t fail_closed_at_window,
+                        int32_t rope_rows) {
+  if (!out || pages_local < 0 || pages_global < 0 || page_size <= 0 || window_left < 0 ||
+      rope_rows <= 0)
+    return PG_KV_ERR_ARG;
+  pg_kv_server* s = new (std::nothrow) pg_kv_server;
+  if (!s) return PG_KV_ERR_ARG;
+  s->page_size = page_size;
+  s->window_left = window_left;
+  s->fail_closed = fail_closed_at_window != 0;
+  s->rope_rows = rope_rows;
+  for (int32_t p = 0; p < pages_local; ++p) s->free_pages[PG_KV_LOCAL].insert(p);
+  for (int32_t p = 0; p < pages_global; ++p) s->free_pages[PG_KV_GLOBAL].insert(p);
+  *out = s;
+  return PG_KV_OK;
+}
+
+void pg_kv_server_destroy(pg_kv_server_t srv) { delete srv; }
+
+int pg_kv_request_open(pg_kv_server_t srv, int64_t* request_id) {
+  if (!srv || !request_id) return PG_KV_ERR_ARG;
+  const int64_t id = srv->next_id++;
+  srv->requests.emplace(id, KvRequest());
+  *request_id = id;
+  return PG_KV_OK;
+}
+
+int pg_kv_request_close(pg_kv_server_t srv, int64_t request_id) {
+  if (!srv) return PG_KV_ERR_ARG;
+  auto it = srv->requests.find(request_id);
+  if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
+  for (int f = 0; f < 2; ++f) srv->give_back(f, it->second.pages[f]);
+  srv->requests.erase(it);
+  return PG_KV_OK;
+}
+
+int pg_kv_admit_step(pg_kv_server_t srv, int64_t request_id, int32_t n_tokens) {
+  if (!srv || n_tokens < 1) return PG_KV_ERR_ARG;
+  auto it = srv->requests.find(request_id);
+  if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
+  KvRequest& r = it->second;
+  // every check before anything changes
+  if (!srv->consistent(r)) return PG_KV_ERR_FRONTIER;
+  const int64_t len = (int64_t)r.frontier[0] + n_tokens;
+  if (len > INT32_MAX) return PG_KV_ERR_ARG;
+  if (srv->fail_closed && len > (int64_t)srv->window_left + 1) return PG_KV_ERR_WINDOW;
+  if (len > srv->rope_rows) return PG_KV_ERR_ROPE;
+  int32_t need[2];
+  for (int f = 0; f < 2; ++f)
+    need[f] = pages_for(len, srv->page_size) - (int32_t)r.pages[f].size();
+  // reserve both before committing either; a refused side drops the other
+  std::vector<int32_t> got[2];
+  if (!srv->reserve(PG_KV_LOCAL, need[PG_KV_LOCAL], &got[PG_KV_LOCAL])) return PG_KV_ERR_NO_PAGES;
+  if (!srv->reserve(PG_KV_GLOBAL, need[PG_KV_GLOBAL], &got[PG_KV_GLOBAL])) {
+    srv->give_back(PG_KV_LOCAL, got[PG_KV_LOCAL]);
+    return PG_KV_ERR_NO_PAGES;
+  }
+  for (int f = 0; f < 2; ++f) {
+    r.pages[f].insert(r.pages[f].end(), got[f].begin(), got[f].end());
+    r.frontier[f] = (int32_t)len;
+  }
+  return PG_KV_OK;
+}
+
+int pg_kv_request_info(pg_kv_server_t srv, int64_t request_id, int32_t* frontier,
+                       int32_t* pages_local, int32_t* pages_global) {
+  if (!srv) return PG_KV_ERR_ARG;
+  auto it = srv->requests.find(request_id);
+  if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
+  if (frontier) *frontier = it->second.frontier[0];
+  if (pages_local) *pages_local = (int32_t)it->second.pages[PG_KV_LOCAL].size();
+  if (pages_global) *pages_global = (int32_t)it->second.pages[PG_KV_GLOBAL].size();
+  return PG_KV_OK;
+}
+
+int pg_kv_request_pages(pg_kv_server_t srv, int64_t request_id, int32_t family, int32_t* out,
+                        int32_t cap, int32_t* n) {
+  if (!srv || !n || (family != PG_KV_LOCAL && family != PG_KV_GLOBAL) || cap < 0)
+    return PG_KV_ERR_ARG;
+  auto it = srv->requests.find(request_id);
+  if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
+  const std::vector<int32_t>& p = it->second.pages[family];
+  if ((int64_t)p.size() > cap) return PG_KV_ERR_CAPACITY;
+  if (!p.empty() && !out) return PG_KV_ERR_ARG;
+  for (size_t i = 0; i < p.size(); ++i) out[i] = p[i];
+  *n = (int32_t)p.size();
+  return PG_KV_OK;
+}
+
+int pg_kv_free_pages(pg_kv_server_t srv, int32_t family, int32_t* n) {
+  if (!srv || !n || (family != PG_KV_LOCAL && family != PG_KV_GLOBAL)) return PG_KV_ERR_ARG;
+  *n = (int32_t)srv->free_pages[family].size();
+  return PG_KV_OK;
+}
+
+int pg_kv_inject_refusal(pg_kv_server_t srv, int32_t family, int32_t count) {
+  if (!srv || (family != PG_KV_LOCAL && family != PG_KV_GLOBAL) || count < 0) return PG_KV_ERR_ARG;
+  srv->refusals[family] = count;
+  return PG_KV_OK;
+}
+
+int pg_kv_batch_plan_inputs(pg_kv_server_t srv, int32_t family, int32_t n,
+                            const int64_t* request_ids, const int32_t* step_tokens,
+                            int64_t* kv_page_indptr, int32_t* page_ids, int32_t cap,
+                            int32_t* last_page_len, int64_t* start_pos, int32_t* n_page_ids) {
+  if (!srv || (family != PG_KV_LOCAL && family != PG_KV_GLOBAL) || n < 0 || cap < 0 ||
+      !n_page_ids || !kv_page_indptr)
+    return PG_KV_ERR_ARG;
+  if (n > 0 && (!request_ids || !step_tokens || !last_page_len || !start_pos))
+    return PG_KV_ERR_ARG;
+  // validate everything first, then write
+  int64_t total = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = srv->requests.find(request_ids[i]);
+    if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
+    const KvRequest& r = it->second;
+    if (!srv->consistent(r)) return PG_KV_ERR_FRONTIER;
+    if (step_tokens[i] < 1 || step_tokens[i] > r.frontier[family]) return PG_KV_ERR_ARG;
+    total += (int64_t)r.pages[family].size();
+  }
+  if (total > cap) return PG_KV_ERR_CAPACITY;
+  if (total > 0 && !page_ids) return PG_KV_ERR_ARG;
+  int64_t off = 0;
+  kv_page_indptr[0] = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const KvRequest& r = srv->requests.find(request_ids[i])->second;
+    const std::vector<int32_t>& p = r.pages[family];
+    for (size_t k = 0; k < p.size(); ++k) page_ids[off + (int64_t)k] = p[k];
+    off += (int64_t)p.size();
+    kv_page_indptr[i + 1] = off;
+    last_page_len[i] = r.frontier[family] - ((int32_t)p.size() - 1) * srv->page_size;
+    start_pos[i] = (int64_t)r.frontier[family] - step_tokens[i];
+  }
+  *n_page_ids = (int32_t)total;
+  return PG_KV_OK;
+}
+
+}  // extern "C"

@@ -255,3 +255,111 @@ EXPORTED = ["pg_plan_paged_prefill", "pg_plan_destroy", "pg_plan_info", "pg_rope
             "pg_prep_paged_hd256", "pg_prep_paged_hd512", "pg_workspace_bytes",
             "pg_attn_paged_prefill", "pg_attn_paged_prefill_hd512", "pg_device_status",
             "pg_launch_count", "pg_status_string"]
+
+
+# ---------------------------------------------------------------- page accounting (include/pg_kv.h)
+PG_KV_OK = 0
+PG_KV_ERR_ARG = -101
+PG_KV_ERR_NO_PAGES = -102
+PG_KV_ERR_WINDOW = -103
+PG_KV_ERR_ROPE = -104
+PG_KV_ERR_FOREIGN = -105
+PG_KV_ERR_FRONTIER = -106
+PG_KV_ERR_CAPACITY = -107
+PG_KV_LOCAL = 0
+PG_KV_GLOBAL = 1
+
+_I32P, _I64P = C.POINTER(C.c_int32), C.POINTER(C.c_int64)
+_lib.pg_kv_server_create.argtypes = [C.POINTER(C.c_void_p), C.c_int32, C.c_int32, C.c_int32,
+                                     C.c_int32, C.c_int32, C.c_int32]
+_lib.pg_kv_server_destroy.argtypes = [C.c_void_p]
+_lib.pg_kv_server_destroy.restype = None
+_lib.pg_kv_request_open.argtypes = [C.c_void_p, _I64P]
+_lib.pg_kv_request_close.argtypes = [C.c_void_p, C.c_int64]
+_lib.pg_kv_admit_step.argtypes = [C.c_void_p, C.c_int64, C.c_int32]
+_lib.pg_kv_request_info.argtypes = [C.c_void_p, C.c_int64, _I32P, _I32P, _I32P]
+_lib.pg_kv_request_pages.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_int32, _I32P]
+_lib.pg_kv_free_pages.argtypes = [C.c_void_p, C.c_int32, _I32P]
+_lib.pg_kv_inject_refusal.argtypes = [C.c_void_p, C.c_int32, C.c_int32]
+_lib.pg_kv_batch_plan_inputs.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                         C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
+                                         _I32P]
+
+
+def pg_kv_server_create(pages_local, pages_global, page_size, window_left, fail_closed_at_window,
+                        rope_rows):
+    """Returns (status, server handle or None)."""
+    h = C.c_void_p()
+    rc = _lib.pg_kv_server_create(C.byref(h), int(pages_local), int(pages_global), int(page_size),
+                                  int(window_left), int(fail_closed_at_window), int(rope_rows))
+    return rc, (h if rc == PG_KV_OK else None)
+
+
+def pg_kv_server_destroy(srv) -> None:
+    _lib.pg_kv_server_destroy(srv)
+
+
+def pg_kv_request_open(srv):
+    """Returns (status, request id)."""
+    rid = C.c_int64()
+    rc = _lib.pg_kv_request_open(srv, C.byref(rid))
+    return rc, rid.value
+
+
+def pg_kv_request_close(srv, request_id) -> int:
+    return _lib.pg_kv_request_close(srv, int(request_id))
+
+
+def pg_kv_admit_step(srv, request_id, n_tokens) -> int:
+    return _lib.pg_kv_admit_step(srv, int(request_id), int(n_tokens))
+
+
+def pg_kv_request_info(srv, request_id):
+    """Returns (status, frontier, pages_local, pages_global)."""
+    f, pl, pg_ = C.c_int32(), C.c_int32(), C.c_int32()
+    rc = _lib.pg_kv_request_info(srv, int(request_id), C.byref(f), C.byref(pl), C.byref(pg_))
+    return rc, f.value, pl.value, pg_.value
+
+
+def pg_kv_request_pages(srv, request_id, family, cap=1 << 20):
+    """Returns (status, int32 array of page ids)."""
+    out = np.empty(max(cap, 1), np.int32)
+    n = C.c_int32()
+    rc = _lib.pg_kv_request_pages(srv, int(request_id), int(family), out.ctypes.data, int(cap),
+                                  C.byref(n))
+    return rc, out[:n.value].copy() if rc == PG_KV_OK else None
+
+
+def pg_kv_free_pages(srv, family):
+    """Returns (status, free page count)."""
+    n = C.c_int32()
+    rc = _lib.pg_kv_free_pages(srv, int(family), C.byref(n))
+    return rc, n.value
+
+
+def pg_kv_inject_refusal(srv, family, count) -> int:
+    return _lib.pg_kv_inject_refusal(srv, int(family), int(count))
+
+
+def pg_kv_batch_plan_inputs(srv, family, request_ids, step_tokens, cap=1 << 20):
+    """Returns (status, kv_page_indptr, page_ids, last_page_len, start_pos) as numpy arrays in
+    pg_plan_paged_prefill's layout."""
+    rids = np.ascontiguousarray(request_ids, np.int64)
+    steps = np.ascontiguousarray(step_tokens, np.int32)
+    n = len(rids)
+    indptr = np.zeros(n + 1, np.int64)
+    pages = np.empty(max(cap, 1), np.int32)
+    last = np.zeros(max(n, 1), np.int32)
+    start = np.zeros(max(n, 1), np.int64)
+    cnt = C.c_int32()
+    rc = _lib.pg_kv_batch_plan_inputs(srv, int(family), n, rids.ctypes.data, steps.ctypes.data,
+                                      indptr.ctypes.data, pages.ctypes.data, int(cap),
+                                      last.ctypes.data, start.ctypes.data, C.byref(cnt))
+    if rc != PG_KV_OK:
+        return rc, None, None, None, None
+    return rc, indptr, pages[:cnt.value].copy(), last[:n].copy(), start[:n].copy()
+
+
+EXPORTED += ["pg_kv_server_create", "pg_kv_server_destroy", "pg_kv_request_open",
+             "pg_kv_request_close", "pg_kv_admit_step", "pg_kv_request_info", "pg_kv_request_pages",
+             "pg_kv_free_pages", "pg_kv_inject_refusal", "pg_kv_batch_plan_inputs"]

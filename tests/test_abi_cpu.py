@@ -1,5 +1,6 @@
 """C-ABI checks that need no GPU: the library loads, exports every declared symbol,
 and rejects bad plans before touching CUDA."""
+import glob
 import os
 import re
 
@@ -8,18 +9,21 @@ import pytest
 import rejects
 from paged_sliding_window_qkv_gb300 import pg
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pg.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(pg_\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    for h in sorted(glob.glob(os.path.join(INCLUDE, "*.h"))):
+        text = open(h).read()
+        names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(pg_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ["pg_plan_paged_prefill", "pg_prep_paged_hd256", "pg_prep_paged_hd512",
-                     "pg_attn_paged_prefill", "pg_attn_paged_prefill_hd512"]:
+                     "pg_attn_paged_prefill", "pg_attn_paged_prefill_hd512", "pg_kv_admit_step"]:
         assert required in names
 
 

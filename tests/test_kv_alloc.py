@@ -1,0 +1,181 @@
+"""Host-side page accounting for two-family paged KV serving (include/pg_kv.h), on CPU.
+
+What is checked follows "feat(gemma4): paged KV serving across both attention families",
+Description and Verification: admission atomic across both pools, the page count as the exact
+frontier account, a forced partial failure leaving both pools at their pre-request occupancy,
+checks before any state change, page ids valid only against the issuing server, and failing
+closed at the sliding window.
+"""
+import numpy as np
+import pytest
+
+from paged_sliding_window_qkv_gb300 import pg
+
+L, G = pg.PG_KV_LOCAL, pg.PG_KV_GLOBAL
+
+
+def server(pages_local=64, pages_global=64, ps=16, window=1023, fail_closed=1, rope_rows=1 << 20):
+    rc, s = pg.pg_kv_server_create(pages_local, pages_global, ps, window, fail_closed, rope_rows)
+    assert rc == pg.PG_KV_OK
+    return s
+
+
+def free(s):
+    return pg.pg_kv_free_pages(s, L)[1], pg.pg_kv_free_pages(s, G)[1]
+
+
+def state(s, rid):
+    rc, f, nl, ng = pg.pg_kv_request_info(s, rid)
+    assert rc == pg.PG_KV_OK
+    return f, nl, ng, tuple(pg.pg_kv_request_pages(s, rid, L)[1]), tuple(pg.pg_kv_request_pages(s, rid, G)[1])
+
+
+def open_req(s):
+    rc, rid = pg.pg_kv_request_open(s)
+    assert rc == pg.PG_KV_OK and rid > 0
+    return rid
+
+
+def test_page_count_is_the_exact_frontier_account():
+    s = server(ps=16)
+    rid = open_req(s)
+    frontier = 0
+    for n in [1, 15, 1, 16, 17, 3, 64, 1]:
+        assert pg.pg_kv_admit_step(s, rid, n) == pg.PG_KV_OK
+        frontier += n
+        f, nl, ng, _, _ = state(s, rid)
+        assert f == frontier
+        assert nl == ng == -(-frontier // 16)        # ceil(frontier / page_size) in both pools
+    assert free(s) == (64 - nl, 64 - ng)
+    pg.pg_kv_server_destroy(s)
+
+
+def test_forced_partial_failure_leaves_both_pools_untouched():
+    # the pages' verification: a refused second family must drop the first family's grant
+    for refused in (G, L):
+        s = server()
+        rid = open_req(s)
+        assert pg.pg_kv_admit_step(s, rid, 20) == pg.PG_KV_OK
+        before_free, before_state = free(s), state(s, rid)
+        assert pg.pg_kv_inject_refusal(s, refused, 1) == pg.PG_KV_OK
+        assert pg.pg_kv_admit_step(s, rid, 30) == pg.PG_KV_ERR_NO_PAGES
+        assert free(s) == before_free
+        assert state(s, rid) == before_state
+        # the refusal was one-shot: the same step is admitted next
+        assert pg.pg_kv_admit_step(s, rid, 30) == pg.PG_KV_OK
+        assert state(s, rid)[0] == 50
+        pg.pg_kv_server_destroy(s)
+
+
+def test_exhausted_family_refuses_without_stranding_the_other():
+    s = server(pages_local=64, pages_global=3, ps=16)
+    rid = open_req(s)
+    assert pg.pg_kv_admit_step(s, rid, 48) == pg.PG_KV_OK       # 3 pages each
+    before = free(s), state(s, rid)
+    assert pg.pg_kv_admit_step(s, rid, 1) == pg.PG_KV_ERR_NO_PAGES   # global has no 4th page
+    assert (free(s), state(s, rid)) == before
+    assert free(s) == (61, 0)
+    pg.pg_kv_server_destroy(s)
+
+
+def test_window_fails_closed_and_rope_bound():
+    s = server(window=31, fail_closed=1, rope_rows=40)
+    rid = open_req(s)
+    assert pg.pg_kv_admit_step(s, rid, 32) == pg.PG_KV_OK        # window_left + 1 positions
+    before = free(s), state(s, rid)
+    assert pg.pg_kv_admit_step(s, rid, 1) == pg.PG_KV_ERR_WINDOW
+    assert (free(s), state(s, rid)) == before
+    pg.pg_kv_server_destroy(s)
+    s = server(window=31, fail_closed=0, rope_rows=40)
+    rid = open_req(s)
+    assert pg.pg_kv_admit_step(s, rid, 40) == pg.PG_KV_OK        # positions 0..39 < rope_rows
+    assert pg.pg_kv_admit_step(s, rid, 1) == pg.PG_KV_ERR_ROPE
+    assert state(s, rid)[0] == 40
+    pg.pg_kv_server_destroy(s)
+
+
+def test_foreign_and_closed_requests_are_refused():
+    s1, s2 = server(), server()
+    r1 = open_req(s1)
+    assert pg.pg_kv_admit_step(s2, r1 + 1000, 1) == pg.PG_KV_ERR_FOREIGN
+    assert pg.pg_kv_admit_step(s1, r1, 17) == pg.PG_KV_OK
+    assert free(s1) == (62, 62)
+    assert pg.pg_kv_request_close(s1, r1) == pg.PG_KV_OK
+    assert free(s1) == (64, 64)                                   # pages returned to both pools
+    assert pg.pg_kv_admit_step(s1, r1, 1) == pg.PG_KV_ERR_FOREIGN
+    assert pg.pg_kv_request_close(s1, r1) == pg.PG_KV_ERR_FOREIGN
+    assert pg.pg_kv_admit_step(s1, 0, 1) == pg.PG_KV_ERR_FOREIGN
+    for s in (s1, s2):
+        pg.pg_kv_server_destroy(s)
+
+
+def test_bad_arguments():
+    assert pg.pg_kv_server_create(4, 4, 0, 10, 1, 100)[0] == pg.PG_KV_ERR_ARG
+    assert pg.pg_kv_server_create(4, 4, 16, -1, 1, 100)[0] == pg.PG_KV_ERR_ARG
+    s = server()
+    rid = open_req(s)
+    assert pg.pg_kv_admit_step(s, rid, 0) == pg.PG_KV_ERR_ARG
+    assert pg.pg_kv_free_pages(s, 2)[0] == pg.PG_KV_ERR_ARG
+    assert pg.pg_kv_admit_step(s, rid, 40) == pg.PG_KV_OK
+    assert pg.pg_kv_request_pages(s, rid, L, cap=2)[0] == pg.PG_KV_ERR_CAPACITY
+    pg.pg_kv_server_destroy(s)
+
+
+def test_batch_plan_inputs_follow_the_plan_contract():
+    ps = 16
+    s = server(ps=ps)
+    rids = [open_req(s) for _ in range(3)]
+    lens = [5, 40, 16]
+    for r, n in zip(rids, lens):
+        assert pg.pg_kv_admit_step(s, r, n) == pg.PG_KV_OK
+    # a decode step of one token each, then the plan inputs for the local family
+    for r in rids:
+        assert pg.pg_kv_admit_step(s, r, 1) == pg.PG_KV_OK
+    rc, indptr, pages, last, start = pg.pg_kv_batch_plan_inputs(s, L, rids, [1, 1, 1])
+    assert rc == pg.PG_KV_OK
+    kv_len = (np.diff(indptr) - 1) * ps + last
+    assert (kv_len == np.array(lens) + 1).all()                    # coverage: kv_len = start + qo_len
+    assert (start + 1 == kv_len).all()
+    assert ((1 <= last) & (last <= ps)).all()
+    assert len(set(pages.tolist())) == len(pages)                  # no page held twice
+    for i, r in enumerate(rids):
+        assert tuple(pages[indptr[i]:indptr[i + 1]]) == tuple(pg.pg_kv_request_pages(s, r, L)[1])
+    # a step longer than the frontier has no plan
+    assert pg.pg_kv_batch_plan_inputs(s, L, rids, [1, 1, 100])[0] == pg.PG_KV_ERR_ARG
+    pg.pg_kv_server_destroy(s)
+
+
+def test_random_traffic_keeps_the_books():
+    rng = np.random.default_rng(11)
+    total = (48, 24)
+    s = server(pages_local=total[0], pages_global=total[1], ps=8, window=1 << 20)
+    live = {}
+    for _ in range(600):
+        op = rng.integers(4)
+        if op == 0 or not live:
+            live[open_req(s)] = 0
+        elif op == 1:
+            r = int(rng.choice(list(live)))
+            assert pg.pg_kv_request_close(s, r) == pg.PG_KV_OK
+            del live[r]
+        else:
+            r = int(rng.choice(list(live)))
+            if rng.random() < 0.1:
+                pg.pg_kv_inject_refusal(s, int(rng.integers(2)), 1)
+            before = free(s), state(s, r)
+            rc = pg.pg_kv_admit_step(s, r, int(rng.integers(1, 20)))
+            if rc != pg.PG_KV_OK:
+                assert rc == pg.PG_KV_ERR_NO_PAGES
+                assert (free(s), state(s, r)) == before
+            pg.pg_kv_inject_refusal(s, 0, 0)
+            pg.pg_kv_inject_refusal(s, 1, 0)
+        # conservation and exclusivity in both pools
+        for fam in (L, G):
+            held = [p for r in live for p in pg.pg_kv_request_pages(s, r, fam)[1]]
+            assert len(held) == len(set(held))
+            assert len(held) + pg.pg_kv_free_pages(s, fam)[1] == total[fam]
+            assert all(0 <= p < total[fam] for p in held)
+        for r in live:
+            f, nl, ng, _, _ = state(s, r)
+            assert nl == ng == -(-f // 8)
+    pg.pg_kv_server_destroy(s)

@@ -1,0 +1,57 @@
+"""Serving two attention families from allocator-issued pages (include/pg_kv.h) on the GPU.
+
+Requests are admitted step by step in both families' pools; each step's plan inputs come from
+the allocator, prep writes K/V into the pages it issued, and attention reads them back. Prep and
+attention are checked against the oracle after a prefill step and a decode step, so the
+page lists, last-page lengths and start positions the allocator produces are exactly what the
+kernels and the oracle agree on.
+"""
+import numpy as np
+import pytest
+
+import parity as PT
+from paged_sliding_window_qkv_gb300 import pg
+from paged_sliding_window_qkv_gb300 import workloads as W
+from paged_sliding_window_qkv_gb300.runner import FamilyRun, device_to_bits
+
+pytestmark = pytest.mark.gpu
+
+PS = 16
+FAMS = {pg.PG_KV_LOCAL: W.HD256, pg.PG_KV_GLOBAL: W.HD512}
+
+
+def step_inputs(srv, fam_id, rids, steps, num_pages, rng, pool_seed):
+    rc, indptr, pages, last, start = pg.pg_kv_batch_plan_inputs(srv, fam_id, rids, steps)
+    assert rc == pg.PG_KV_OK
+    qo = np.zeros(len(rids) + 1, np.int64)
+    qo[1:] = np.cumsum(steps)
+    b = W.Batch(qo, indptr, pages, last, start, PS, num_pages)
+    return W.family_inputs(rng, FAMS[fam_id], b, 1, 0, "sentinel", pool_seed)
+
+
+def test_allocator_pages_drive_prep_and_attention():
+    num_pages = 24
+    rc, srv = pg.pg_kv_server_create(num_pages, num_pages, PS, 1023, 1, 4096)
+    assert rc == pg.PG_KV_OK
+    rids = [pg.pg_kv_request_open(srv)[1] for _ in range(3)]
+    rng = np.random.Generator(np.random.PCG64(2024))
+    pools = {}
+    for steps in ([37, 20, 16], [1, 1, 1]):            # a prefill step, then a decode step
+        for r, n in zip(rids, steps):
+            assert pg.pg_kv_admit_step(srv, r, n) == pg.PG_KV_OK
+        for fam_id in (pg.PG_KV_LOCAL, pg.PG_KV_GLOBAL):
+            fi = step_inputs(srv, fam_id, rids, steps, num_pages, rng, 7)
+            before = pools.get(fam_id)
+            run = FamilyRun(fi, pool_bits=before, rope_rows=4096)
+            run.prep()
+            run.attn()
+            pools[fam_id] = device_to_bits(run.pool)
+            assert pg.pg_device_status() == pg.PG_OK
+            PT.check_prep(run, fi, initial_pool_bits=before)
+            ref = PT.attn_reference(fi, device_to_bits(run.q_out), pools[fam_id])
+            PT.attn_gate(PT.bf16_out(run), ref, f"family {fam_id} steps {steps}")
+            run.close()
+    for r in rids:
+        assert pg.pg_kv_request_close(srv, r) == pg.PG_KV_OK
+    assert pg.pg_kv_free_pages(srv, pg.PG_KV_LOCAL)[1] == num_pages
+    pg.pg_kv_server_destroy(srv)
