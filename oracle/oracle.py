@@ -118,13 +118,22 @@ def token_request_and_position(qo_indptr, start_pos):
     return req, start_pos[req] + local
 
 
-def slot_of(req, pos, kv_page_indptr, page_ids, page_size: int):
-    """(physical page id, in-page slot) holding KV position ``pos`` of ``req``."""
+def slot_of(req, pos, kv_page_indptr, page_ids, page_size: int, ring: bool = False):
+    """(physical page id, in-page slot) holding KV position ``pos`` of ``req``.
+
+    With ``ring`` the request's pages form a ring ("serving prep needs pool-write forms",
+    Proposed Plan: window-crossing callers need a separate slot mapping): logical page
+    pos // page_size lives in the request's page (pos // page_size) mod (pages held), so a
+    position reuses the slot of the position one ring length (pages x page_size) earlier.
+    """
     kv_page_indptr = np.asarray(kv_page_indptr, dtype=np.int64)
     page_ids = np.asarray(page_ids, dtype=np.int64)
     req = np.asarray(req, dtype=np.int64)
     pos = np.asarray(pos, dtype=np.int64)
-    return page_ids[kv_page_indptr[req] + pos // page_size], pos % page_size
+    logical = pos // page_size
+    if ring:
+        logical = logical % (kv_page_indptr[req + 1] - kv_page_indptr[req])
+    return page_ids[kv_page_indptr[req] + logical], pos % page_size
 
 
 def pool_row_offset(layer, page, kv, head, slot, num_pages: int, num_kv_heads: int,
@@ -170,9 +179,9 @@ def prep_hd512(q_raw, k_raw, w_q, w_k, eps, positions, theta):
 
 
 def prep_pool_writes(req, pos, kv_page_indptr, page_ids, page_size, layer, num_pages,
-                     num_kv_heads, head_dim):
+                     num_kv_heads, head_dim, ring: bool = False):
     """Element offsets [T, 2, Hkv] of the K and V rows each token writes."""
-    page, slot = slot_of(req, pos, kv_page_indptr, page_ids, page_size)
+    page, slot = slot_of(req, pos, kv_page_indptr, page_ids, page_size, ring)
     kv = np.arange(2, dtype=np.int64)[None, :, None]
     head = np.arange(num_kv_heads, dtype=np.int64)[None, None, :]
     return pool_row_offset(layer, page[:, None, None], kv, head, slot[:, None, None],
@@ -194,10 +203,17 @@ def visible(p, j, window_left: int):
     return m
 
 
-def gather_kv(pool_bits: np.ndarray, layer: int, pages_of_req, kv_len: int, page_size: int):
-    """K and V of positions [0, kv_len) of one request, fp64 [kv_len, Hkv, D] each."""
+def gather_kv(pool_bits: np.ndarray, layer: int, pages_of_req, kv_len: int, page_size: int,
+              ring: bool = False):
+    """K and V of positions [0, kv_len) of one request, fp64 [kv_len, Hkv, D] each. With
+    ``ring`` (see slot_of) a position older than one ring length reads whatever newer position
+    now holds its slot; the window mask keeps such keys out of every softmax."""
     j = np.arange(kv_len, dtype=np.int64)
-    pages = np.asarray(pages_of_req, dtype=np.int64)[j // page_size]
+    pages_of_req = np.asarray(pages_of_req, dtype=np.int64)
+    logical = j // page_size
+    if ring:
+        logical = logical % len(pages_of_req)
+    pages = pages_of_req[logical]
     slots = j % page_size
     k = bf16_to_f64(pool_bits[layer, pages, 0, :, slots, :])
     v = bf16_to_f64(pool_bits[layer, pages, 1, :, slots, :])
@@ -218,11 +234,12 @@ def attend_rows(q_rows, p_rows, k, v, window_left: int, sm_scale: float):
 
 def attention(q_bits, pool_bits, layer: int, qo_indptr, kv_page_indptr, page_ids,
               last_page_len, start_pos, num_kv_heads: int, window_left: int,
-              sm_scale: float, rows=None, row_chunk: int = 512):
+              sm_scale: float, rows=None, row_chunk: int = 512, ring: bool = False):
     """Paged prefill attention over a page table (fp64).
 
     q_bits: bf16 bits [T, Hq, D]; pool_bits: bf16 bits [L, P, 2, Hkv, ps, D].
-    The kv length of request r is (pages_r - 1) * ps + last_page_len_r, and its
+    The kv length of request r is (pages_r - 1) * ps + last_page_len_r (with ``ring``:
+    start_pos_r + qo_len_r, the pages forming a ring, see slot_of), and its
     queries sit at positions start_pos_r + t. Query head h reads KV head
     h // (Hq / Hkv). ``rows``: optional int array [n, 2] of (token, head) to
     evaluate; returns fp64 [n, D]. Without it returns fp64 [T, Hq, D].
@@ -230,7 +247,8 @@ def attention(q_bits, pool_bits, layer: int, qo_indptr, kv_page_indptr, page_ids
     qo_indptr = np.asarray(qo_indptr, dtype=np.int64)
     kv_page_indptr = np.asarray(kv_page_indptr, dtype=np.int64)
     page_ids = np.asarray(page_ids, dtype=np.int64)
-    last_page_len = np.asarray(last_page_len, dtype=np.int64)
+    if not ring:
+        last_page_len = np.asarray(last_page_len, dtype=np.int64)
     T, Hq, D = q_bits.shape
     ps = pool_bits.shape[4]
     group = Hq // num_kv_heads
@@ -244,9 +262,12 @@ def attention(q_bits, pool_bits, layer: int, qo_indptr, kv_page_indptr, page_ids
     sel_req = req_of[sel[:, 0]] if len(sel) else np.zeros(0, np.int64)
     for r in np.unique(sel_req):
         npages = kv_page_indptr[r + 1] - kv_page_indptr[r]
-        kv_len = int((npages - 1) * ps + last_page_len[r])
+        if ring:
+            kv_len = int(np.asarray(start_pos, np.int64)[r] + qo_indptr[r + 1] - qo_indptr[r])
+        else:
+            kv_len = int((npages - 1) * ps + last_page_len[r])
         k, v = gather_kv(pool_bits, layer, page_ids[kv_page_indptr[r]:kv_page_indptr[r + 1]],
-                         kv_len, ps)
+                         kv_len, ps, ring)
         idx_r = np.nonzero(sel_req == r)[0]
         for g in range(num_kv_heads):
             idx = idx_r[(sel[idx_r, 1] // group) == g]
