@@ -49,11 +49,11 @@ enum {
   PG_ERR_HEADS = -6,          /* num_qo_heads <= 0, num_kv_heads < 0 or num_qo_heads % num_kv_heads != 0 */
   PG_ERR_NONFINITE = -7,      /* sm_scale or eps not finite, or eps <= 0, or theta <= 0        */
   PG_ERR_ROPE_RANGE = -8,     /* a query position at or past rope_rows ([P2] Proposed Plan)   */
-  PG_ERR_COVERAGE = -9,       /* pages do not cover exactly [0, start_pos + qo_len)            */
+  PG_ERR_COVERAGE = -9,       /* pages do not cover exactly [0, start_pos + qo_len) (ring: the window plus the step) */
   PG_ERR_LAYER = -10,         /* layer outside [0, num_layers)                                 */
   PG_ERR_LAYOUT = -11,        /* pool strides / capacity / head geometry inconsistent          */
   PG_ERR_PLAN_MISMATCH = -12, /* plan heads, head_dim, page_size or cta_tile_q disagree        */
-  PG_ERR_WINDOW = -13,        /* window_left < -1                                              */
+  PG_ERR_WINDOW = -13,        /* window_left < -1, or outside [0, plan window] on a ring plan  */
   PG_ERR_WORKSPACE = -14,     /* workspace null or smaller than pg_workspace_bytes             */
   PG_ERR_STREAM = -15,        /* call stream differs from the plan's stream ([P3] review)      */
   PG_ERR_CUDA = -16,          /* a CUDA runtime call failed                                    */
@@ -116,6 +116,32 @@ int pg_plan_paged_prefill(pg_plan_t* plan, int32_t num_req, const int64_t* qo_in
                           const int32_t* last_page_len, const int64_t* start_pos,
                           int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                           int32_t page_size, pg_stream_t stream);
+
+/*
+ * pg_plan_paged_prefill_ring -- the same plan for window-crossing requests, with ring
+ * slot addressing ([P2] Proposed Plan: slots equal positions only below the sliding
+ * window, and callers that cross it need a separate slot mapping). Request r holds
+ * pages_r = kv_page_indptr[r+1] - kv_page_indptr[r] pages as a ring: position p lives
+ * in page page_ids[kv_page_indptr[r] + (p / page_size) mod pages_r], slot
+ * p mod page_size. Prep writes the step's K/V there; attention reads keys
+ * [max(0, p - window_left), p] of each query position p from the same slots.
+ *
+ * Inputs as for pg_plan_paged_prefill, without last_page_len (the ring has no last page):
+ *   window_left  >= 0: the largest window attention may run with on this plan.
+ * Coverage: pages_r * page_size >= window_left + qo_len_r for every request, so no key
+ * that a query of the step can see is overwritten by the step's own writes
+ * (PG_ERR_COVERAGE otherwise); window_left < 0 fails with PG_ERR_WINDOW. A request may
+ * start at any position (start_pos is not bounded by its pages), and all positions
+ * below start_pos_r must have been written through the same ring by earlier steps.
+ * Attention on a ring plan requires 0 <= window_left <= the plan's window
+ * (PG_ERR_WINDOW otherwise). Everything else (stream binding, in-place update, checks)
+ * is as for pg_plan_paged_prefill.
+ */
+int pg_plan_paged_prefill_ring(pg_plan_t* plan, int32_t num_req, const int64_t* qo_indptr,
+                               const int64_t* kv_page_indptr, const int32_t* page_ids,
+                               const int64_t* start_pos, int32_t num_qo_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                               int32_t window_left, pg_stream_t stream);
 
 /* Free a plan (host and device storage; device frees are ordered on its stream). NULL is a no-op. */
 void pg_plan_destroy(pg_plan_t plan);

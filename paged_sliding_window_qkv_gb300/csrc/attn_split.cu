@@ -134,8 +134,9 @@ attn_split_kernel(AttnArgs a) {
   if (!C::DECODE) ntok = min(a.cta_tile_q, qo_len - tok0);
   const int32_t kvp0 = pl.kv_page_indptr[r], kvp1 = pl.kv_page_indptr[r + 1];
   const int32_t ps = a.pool.page_size;
-  const int32_t kv_len = (kvp1 - kvp0 - 1) * ps + pl.last_page_len[r];
   const int32_t sp = pl.start_pos[r];
+  // ring addressing (window-crossing requests): every position below start + qo_len is held
+  const int32_t kv_len = pl.ring ? sp + qo_len : (kvp1 - kvp0 - 1) * ps + pl.last_page_len[r];
   const int32_t p_first = sp + tok0, p_last = sp + tok0 + ntok - 1;
   const int32_t W = a.window_left;
   int32_t lo = W >= 0 ? max(0, p_first - W) : 0;
@@ -173,7 +174,8 @@ attn_split_kernel(AttnArgs a) {
     bool valid = j < hi;
     const __nv_bfloat16* src = a.pool.layer_base;
     if (valid) {
-      const int32_t pidx = kvp0 + j / ps;
+      const int32_t lp = j / ps;  // logical page; ring addressing wraps it over the pages held
+      const int32_t pidx = kvp0 + (pl.ring ? lp % max(kvp1 - kvp0, 1) : lp);
       const int32_t page = pidx < kvp1 ? pl.page_ids[pidx] : -1;
       if (page < 0 || page >= a.pool.num_pages) {
         if (c0 == 0) atomicOr(a.status, kStatusBounds);
@@ -394,8 +396,9 @@ attn_merge_kernel(AttnArgs a) {
   const int32_t r = blockIdx.x, h = blockIdx.y;
   const PlanDev& pl = a.plan;
   const int32_t kvp0 = pl.kv_page_indptr[r], kvp1 = pl.kv_page_indptr[r + 1];
-  const int32_t kv_len = (kvp1 - kvp0 - 1) * a.pool.page_size + pl.last_page_len[r];
   const int32_t p = pl.start_pos[r];
+  const int32_t kv_len = pl.ring ? p + (pl.qo_indptr[r + 1] - pl.qo_indptr[r])
+                                 : (kvp1 - kvp0 - 1) * a.pool.page_size + pl.last_page_len[r];
   const int32_t W = a.window_left;
   const int32_t lo = W >= 0 ? max(0, p - W) : 0;
   const int32_t hi = min(p + 1, kv_len);

@@ -508,7 +508,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!box_lane) return -1;
         const int32_t ks = u.kb0 + t * kBN + key_off + my_box * BR;
         if (ks >= u.kv_len) return -1;
-        const int32_t pidx = u.kvp0 + ks / ps;
+        const int32_t lp = ks / ps;  // logical page; ring addressing wraps it over the pages held
+        const int32_t pidx = u.kvp0 + (pl.ring ? lp % max(u.kvp1 - u.kvp0, 1) : lp);
         return (pidx < u.kvp1 && pidx < pl.num_page_ids) ? pl.page_ids[pidx] : a.num_pages;
       };
       auto issue_part = [&](int s, int round, int c0, int32_t t, int32_t page) -> bool {

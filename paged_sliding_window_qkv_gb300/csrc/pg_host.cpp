@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <algorithm>
 #include <vector>
 
 namespace pg {
@@ -69,6 +70,7 @@ struct pg_plan {
           max_pos_end = 0;
   int32_t cta_tile_q = 0, decode = 0, kv_chunk = 0, max_chunks = 0, num_work = 0, num_pairs = 0;
   int32_t num_page_ids = 0;
+  int32_t ring = 0, ring_window = -1;  // ring addressing (window-crossing requests) and its window
   cudaStream_t stream = nullptr;
   int device = 0;
   int32_t* dev = nullptr;  // one device allocation holding every metadata array
@@ -80,16 +82,25 @@ struct pg_plan {
 
 namespace {
 
+// ring_window < 0: linear addressing (slot = position, pages cover [0, kv_len) exactly, with
+// last_page_len). ring_window >= 0: ring addressing for window-crossing requests: logical page
+// pos / ps lives in the request's page (pos / ps) mod (pages held), kv_len = start_pos + qo_len,
+// last_page_len is not read, and the ring must hold the window plus the step
+// (pages * ps >= ring_window + qo_len), so no key a query of the step can see is overwritten by
+// the step's own writes.
 int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
                const int64_t* kv_page_indptr, const int32_t* page_ids,
                const int32_t* last_page_len, const int64_t* start_pos, int32_t Hq,
-               int32_t Hkv, int32_t D, int32_t ps, cudaStream_t stream) {
+               int32_t Hkv, int32_t D, int32_t ps, cudaStream_t stream,
+               int32_t ring_window = -1) {
+  const bool ring = ring_window >= 0;
   // The head relation is settled before anything divides by num_kv_heads.
   if (Hkv == 0) return PG_ERR_ZERO_KV_HEADS;
   if (Hkv < 0 || Hq <= 0 || Hq % Hkv != 0) return PG_ERR_HEADS;
   if (D <= 0 || D % 2 != 0 || ps <= 0) return PG_ERR_ARG;
   if (num_req < 0) return PG_ERR_ARG;
-  if (num_req > 0 && (!qo_indptr || !kv_page_indptr || !page_ids || !last_page_len || !start_pos))
+  if (num_req > 0 && (!qo_indptr || !kv_page_indptr || !page_ids || !start_pos ||
+                      (!ring && !last_page_len)))
     return PG_ERR_ARG;
   const int32_t group = Hq / Hkv;
 
@@ -109,13 +120,24 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
     if (sp < 0) return PG_ERR_ARG;
     int64_t pos_end = 0;
     if (!add_i64(sp, qo_len, &pos_end) || !fits_i32(pos_end)) return PG_ERR_I32_OVERFLOW;
-    const int32_t lpl = last_page_len[r];
-    if (lpl < 1 || lpl > ps) return PG_ERR_LAST_PAGE_LEN;
+    int32_t lpl = 0;
     int64_t kv_len = 0;
-    if (!mul_i64(k1 - k0 - 1, ps, &kv_len) || !add_i64(kv_len, lpl, &kv_len))
-      return PG_ERR_I32_OVERFLOW;
-    if (!fits_i32(kv_len)) return PG_ERR_I32_OVERFLOW;
-    if (kv_len != pos_end) return PG_ERR_COVERAGE;
+    if (!ring) {
+      lpl = last_page_len[r];
+      if (lpl < 1 || lpl > ps) return PG_ERR_LAST_PAGE_LEN;
+      if (!mul_i64(k1 - k0 - 1, ps, &kv_len) || !add_i64(kv_len, lpl, &kv_len))
+        return PG_ERR_I32_OVERFLOW;
+      if (!fits_i32(kv_len)) return PG_ERR_I32_OVERFLOW;
+      if (kv_len != pos_end) return PG_ERR_COVERAGE;
+    } else {
+      int64_t cap = 0, need = 0;
+      if (!mul_i64(k1 - k0, ps, &cap) || !add_i64(ring_window, qo_len, &need))
+        return PG_ERR_I32_OVERFLOW;
+      if (cap < need) return PG_ERR_COVERAGE;  // the ring cannot hold the window plus the step
+      kv_len = pos_end;
+      // the position's slot in its (ring) page; last_page_len is not used in ring addressing
+      lpl = (int32_t)(pos_end - ((pos_end - 1) / ps) * ps);
+    }
     qo[r + 1] = (int32_t)q1;
     kvp[r + 1] = (int32_t)k1;
     last[r] = lpl;
@@ -148,7 +170,7 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
       // the tcgen05 prefill runs query tiles in pairs (one per CTA of a cluster) that share
       // their key tiles; a request with an odd number of tiles ends with a single-tile pair
       for (int64_t t = 0; t < len; t += 2 * (int64_t)cta) {
-        const int32_t kv_len = (kvp[r + 1] - kvp[r] - 1) * ps + last[r];
+        const int32_t kv_len = ring ? start[r] + len : (kvp[r + 1] - kvp[r] - 1) * ps + last[r];
         const int32_t e[8] = {(int32_t)t, qo[r], len, start[r], kvp[r], kvp[r + 1], kv_len, r};
         ptab.insert(ptab.end(), e, e + 8);
       }
@@ -200,7 +222,11 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   q.max_page_id = max_page; q.max_last_page_len = max_last; q.max_qo_len = max_qo;
   q.max_kv_len = max_kv; q.max_pos_end = max_end;
   q.cta_tile_q = cta; q.decode = all_one ? 1 : 0; q.kv_chunk = chunk;
-  q.max_chunks = max_kv > 0 ? (max_kv + chunk - 1) / chunk : 0;
+  // decode partials: a query sees at most window + 1 keys in ring addressing
+  const int64_t seen = ring ? std::min<int64_t>(max_kv, (int64_t)ring_window + 1) : max_kv;
+  q.max_chunks = seen > 0 ? (int32_t)((seen + chunk - 1) / chunk) : 0;
+  q.ring = ring ? 1 : 0;
+  q.ring_window = ring ? ring_window : -1;
   q.num_work = (int32_t)nwork; q.num_pairs = (int32_t)(ptab.size() / 8); q.num_page_ids = NP;
   q.stream = stream; q.device = dev;
   q.dev = d; q.dev_elems = host.size();
@@ -228,6 +254,7 @@ PlanDev plan_dev(const pg_plan* p) {
   v.num_page_ids = p->num_page_ids;
   v.num_work = p->num_work;
   v.num_pairs = p->num_pairs;
+  v.ring = p->ring;
   return v;
 }
 
@@ -346,6 +373,8 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
   if (kernel_cta == 0 || kernel_cta != plan->cta_tile_q) return PG_ERR_PLAN_MISMATCH;
   if (attn_kernel_kv_chunk(D) != plan->kv_chunk) return PG_ERR_PLAN_MISMATCH;
   if (window_left < -1) return PG_ERR_WINDOW;
+  // ring addressing holds only the window the plan was built for
+  if (plan->ring && (window_left < 0 || window_left > plan->ring_window)) return PG_ERR_WINDOW;
   if (!std::isfinite(sm_scale)) return PG_ERR_NONFINITE;
   if (!plan->decode && attn_tc_supported(D, group, plan->page_size) &&
       (int64_t)pool->num_pages * 2 * pool->num_kv_heads * pool->page_size > INT32_MAX)
@@ -420,6 +449,31 @@ int pg_plan_paged_prefill(pg_plan_t* plan, int32_t num_req, const int64_t* qo_in
   if (!p) return PG_ERR_ARG;
   int rc = build_plan(p, num_req, qo_indptr, kv_page_indptr, page_ids, last_page_len, start_pos,
                       num_qo_heads, num_kv_heads, head_dim, page_size, s);
+  if (rc != PG_OK) {
+    delete p;
+    return rc;
+  }
+  *plan = p;
+  return PG_OK;
+}
+
+int pg_plan_paged_prefill_ring(pg_plan_t* plan, int32_t num_req, const int64_t* qo_indptr,
+                               const int64_t* kv_page_indptr, const int32_t* page_ids,
+                               const int64_t* start_pos, int32_t num_qo_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                               int32_t window_left, pg_stream_t stream) {
+  if (!plan) return PG_ERR_ARG;
+  if (window_left < 0) return PG_ERR_WINDOW;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (*plan) {
+    if ((*plan)->stream != s) return PG_ERR_STREAM;
+    return build_plan(*plan, num_req, qo_indptr, kv_page_indptr, page_ids, nullptr, start_pos,
+                      num_qo_heads, num_kv_heads, head_dim, page_size, s, window_left);
+  }
+  pg_plan* p = new (std::nothrow) pg_plan();
+  if (!p) return PG_ERR_ARG;
+  int rc = build_plan(p, num_req, qo_indptr, kv_page_indptr, page_ids, nullptr, start_pos,
+                      num_qo_heads, num_kv_heads, head_dim, page_size, s, window_left);
   if (rc != PG_OK) {
     delete p;
     return rc;

@@ -22,6 +22,9 @@ struct PlanDev {
   // qo_len, start_pos, kv_page_indptr[r], kv_page_indptr[r + 1], kv_len, r}
   const int32_t* pair_tab;
   int32_t num_req, num_tokens, num_page_ids, num_work, num_pairs;
+  // ring addressing: logical page pos / page_size of request r is its page
+  // (pos / page_size) mod (pages of r), and kv_len = start_pos + qo_len
+  int32_t ring;
 };
 
 // Device view of one family's pool, already narrowed to the called layer.

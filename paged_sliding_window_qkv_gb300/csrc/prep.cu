@@ -124,10 +124,12 @@ __device__ __forceinline__ bool token_meta(const PrepArgs& a, int32_t t, TokMeta
   const int32_t q0 = pl.qo_indptr[r];
   const int32_t pos = pl.start_pos[r] + (t - q0);
   const int32_t ps = a.pool.page_size;
-  const int32_t pidx = pl.kv_page_indptr[r] + pos / ps;
-  if (t < q0 || t >= pl.qo_indptr[r + 1] || pos < 0 || pos >= a.rope_rows ||
-      pidx >= pl.kv_page_indptr[r + 1] || pidx >= pl.num_page_ids)
+  const int32_t kvp0 = pl.kv_page_indptr[r], npg = pl.kv_page_indptr[r + 1] - kvp0;
+  if (t < q0 || t >= pl.qo_indptr[r + 1] || pos < 0 || pos >= a.rope_rows || npg <= 0)
     return false;
+  // ring addressing: logical page pos / ps lives in page (pos / ps) mod (pages held)
+  const int32_t pidx = kvp0 + (pl.ring ? (pos / ps) % npg : pos / ps);
+  if (pidx >= kvp0 + npg || pidx >= pl.num_page_ids) return false;
   const int32_t page = pl.page_ids[pidx];
   if (page < 0 || page >= a.pool.num_pages) return false;
   m->pos = pos;

@@ -83,6 +83,8 @@ def _sig(name, res, *args):
 
 _plan = _sig("pg_plan_paged_prefill", C.c_int, C.POINTER(_P), _I32, _P, _P, _P, _P, _P,
              _I32, _I32, _I32, _I32, _P)
+_plan_ring = _sig("pg_plan_paged_prefill_ring", C.c_int, C.POINTER(_P), _I32, _P, _P, _P, _P,
+                  _I32, _I32, _I32, _I32, _I32, _P)
 _destroy = _sig("pg_plan_destroy", None, _P)
 _info = _sig("pg_plan_info", C.c_int, _P, C.POINTER(pg_plan_info_t))
 _rope = _sig("pg_rope_table", C.c_int, _P, _P, _I32, _I32, _F64, _P)
@@ -189,6 +191,23 @@ def pg_plan_paged_prefill(plan, num_req, qo_indptr, kv_page_indptr, page_ids, la
     return rc, (Plan(h.value) if rc == PG_OK else None)
 
 
+def pg_plan_paged_prefill_ring(plan, num_req, qo_indptr, kv_page_indptr, page_ids, start_pos,
+                               num_qo_heads, num_kv_heads, head_dim, page_size, window_left,
+                               stream=None):
+    """Build (plan=None) or update (plan=Plan) a ring-addressed plan. Returns (status, Plan
+    or None)."""
+    h = _P(plan.handle if plan is not None else None)
+    keep = [_host(qo_indptr, np.int64), _host(kv_page_indptr, np.int64),
+            _host(page_ids, np.int32), _host(start_pos, np.int64)]
+    rc = _plan_ring(C.byref(h), int(num_req), *[k[1] for k in keep], int(num_qo_heads),
+                    int(num_kv_heads), int(head_dim), int(page_size), int(window_left),
+                    _stream(stream))
+    del keep
+    if plan is not None:
+        return rc, plan
+    return rc, (Plan(h.value) if rc == PG_OK else None)
+
+
 def pg_workspace_bytes(plan) -> int:
     return int(_wsb(plan.handle if plan is not None else None))
 
@@ -251,7 +270,7 @@ def pg_attn_paged_decode_noalloc(plan, pool: pg_pool_t, layer, q, out, window_le
                          _ptr(q), _ptr(out), int(window_left), float(sm_scale), _stream(stream))
 
 
-EXPORTED = ["pg_plan_paged_prefill", "pg_plan_destroy", "pg_plan_info", "pg_rope_table",
+EXPORTED = ["pg_plan_paged_prefill", "pg_plan_paged_prefill_ring", "pg_plan_destroy", "pg_plan_info", "pg_rope_table",
             "pg_prep_paged_hd256", "pg_prep_paged_hd512", "pg_workspace_bytes",
             "pg_attn_paged_prefill", "pg_attn_paged_prefill_hd512", "pg_device_status",
             "pg_launch_count", "pg_status_string"]

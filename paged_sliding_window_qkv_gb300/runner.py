@@ -27,7 +27,7 @@ class FamilyRun:
     """Everything one family's prep + attention needs, resident on the GPU."""
 
     def __init__(self, fi: FamilyInputs, device="cuda", stream=None, pool_bits=None,
-                 rope_rows: int | None = None):
+                 rope_rows: int | None = None, ring_window: int | None = None):
         self.fi = fi
         f, b = fi.family, fi.batch
         self.D, self.Hq, self.Hkv = f.head_dim, f.num_qo_heads, f.num_kv_heads
@@ -50,10 +50,15 @@ class FamilyRun:
         self.rope_sin = torch.empty(self.rope_rows, half, dtype=torch.float32, device=device)
         pg.check(pg.pg_rope_table(self.rope_cos, self.rope_sin, self.rope_rows, self.D,
                                   f.rope_theta, stream), "pg_rope_table")
-        rc, self.plan = pg.pg_plan_paged_prefill(
-            None, b.num_req, b.qo_indptr, b.kv_page_indptr, b.page_ids, b.last_page_len,
-            b.start_pos, self.Hq, self.Hkv, self.D, b.page_size, stream)
-        pg.check(rc, "pg_plan_paged_prefill")
+        if ring_window is None:
+            rc, self.plan = pg.pg_plan_paged_prefill(
+                None, b.num_req, b.qo_indptr, b.kv_page_indptr, b.page_ids, b.last_page_len,
+                b.start_pos, self.Hq, self.Hkv, self.D, b.page_size, stream)
+        else:   # ring slot addressing for window-crossing requests
+            rc, self.plan = pg.pg_plan_paged_prefill_ring(
+                None, b.num_req, b.qo_indptr, b.kv_page_indptr, b.page_ids, b.start_pos,
+                self.Hq, self.Hkv, self.D, b.page_size, ring_window, stream)
+        pg.check(rc, "plan")
         T = b.num_tokens
         self.q_out = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=device)
         self.out = torch.empty(T, self.Hq, self.D, dtype=torch.bfloat16, device=device)

@@ -45,7 +45,7 @@ def attn_gate(gpu, ref, what=""):
     return mx, mean
 
 
-def prep_reference(fi: W.FamilyInputs):
+def prep_reference(fi: W.FamilyInputs, ring: bool = False):
     """Oracle prep outputs (fp64) and the pool row offsets each token writes."""
     f, b = fi.family, fi.batch
     req, pos = O.token_request_and_position(b.qo_indptr, b.start_pos)
@@ -57,16 +57,16 @@ def prep_reference(fi: W.FamilyInputs):
     else:
         qo, ko, vo = O.prep_hd512(q, k, wq, wk, fi.eps, pos, f.rope_theta)
     offs = O.prep_pool_writes(req, pos, b.kv_page_indptr, b.page_ids, b.page_size, fi.layer,
-                              b.num_pages, f.num_kv_heads, f.head_dim)
+                              b.num_pages, f.num_kv_heads, f.head_dim, ring=ring)
     return qo, ko, vo, offs
 
 
-def check_prep(run, fi: W.FamilyInputs, initial_pool_bits=None):
+def check_prep(run, fi: W.FamilyInputs, initial_pool_bits=None, ring: bool = False):
     """Compare q_out and the pool after prep with the oracle; untouched rows byte-exact."""
     torch.cuda.synchronize()
     f = fi.family
     D = f.head_dim
-    qo, ko, vo, offs = prep_reference(fi)
+    qo, ko, vo, offs = prep_reference(fi, ring)
     frac_q = prep_gate(device_to_bits(run.q_out), qo, "q_out")
     rows_dev = run.pool.view(-1, D)
     row_idx = torch.from_numpy((offs // D).reshape(-1)).to(rows_dev.device)
@@ -88,12 +88,13 @@ def check_prep(run, fi: W.FamilyInputs, initial_pool_bits=None):
     return frac_q, frac_k, frac_v
 
 
-def attn_reference(fi: W.FamilyInputs, q_bits, pool_bits, window_left=None, rows=None):
+def attn_reference(fi: W.FamilyInputs, q_bits, pool_bits, window_left=None, rows=None,
+                   ring: bool = False):
     b = fi.batch
     w = fi.family.window_left if window_left is None else window_left
     return O.attention(q_bits, pool_bits, fi.layer, b.qo_indptr, b.kv_page_indptr, b.page_ids,
                        b.last_page_len, b.start_pos, fi.family.num_kv_heads, w, fi.sm_scale,
-                       rows=rows)
+                       rows=rows, ring=ring)
 
 
 def bf16_out(run):

@@ -4,6 +4,7 @@ import glob
 import os
 import re
 
+import numpy as np
 import pytest
 
 import rejects
@@ -83,3 +84,20 @@ def test_null_plan_is_rejected_everywhere():
     assert pg.pg_attn_paged_prefill_hd512(None, d, 0, 0, 0, -1, 1.0, None, 0, 0) == pg.PG_ERR_ARG
     assert pg.pg_workspace_bytes(None) == 0
     assert pg.pg_rope_table(0, 0, 4, 256, 1e4, 0) == pg.PG_ERR_ARG
+
+
+def _ring_plan(pages, qo_len, start, window_left, ps=16):
+    return pg.pg_plan_paged_prefill_ring(
+        None, 1, np.array([0, qo_len], np.int64), np.array([0, pages], np.int64),
+        np.arange(pages, dtype=np.int32), np.array([start], np.int64), 16, 8, 256, ps,
+        window_left, stream=0)
+
+
+def test_ring_plan_rejects_before_touching_cuda():
+    # the ring must hold the window plus the step: 8 pages x 16 = 128 >= 100 + 28, not + 29
+    before = pg.pg_launch_count()
+    assert _ring_plan(8, 29, 5000, 100)[0] == pg.PG_ERR_COVERAGE
+    assert _ring_plan(8, 29, 5000, 100)[1] is None
+    assert _ring_plan(8, 1, 0, -1)[0] == pg.PG_ERR_WINDOW
+    assert _ring_plan(0, 1, 0, 0)[0] == pg.PG_ERR_ARG          # a request with no pages
+    assert pg.pg_launch_count() == before
