@@ -78,12 +78,15 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 template <int DQK>
 struct TcCfg {
   static constexpr int KP = DQK / 256;                // K parts per tile (256 d each)
-  static constexpr int NKS = DQK == 256 ? 6 : 5;      // K part slots
+  static constexpr int NKS = DQK == 256 ? 6 : 6;      // K part slots
   static constexpr int NVR = DQK == 256 ? 6 : 3;      // V tile slots
   static constexpr int NS = NKS + NVR;
   static constexpr int QS_BYTES = (DQK - 256) * kM * 2;  // Q columns past 256, in shared memory
   static constexpr int P_BUF = kM * kBN * 2;          // one P buffer: 128 rows x 64 keys bf16
-  static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes + 2 * P_BUF;
+  // P buffers: head_dim 512 keeps one (PV(j) has long completed when the softmax of tile j + 1
+  // writes P) and gives the 16 KB to the K ring
+  static constexpr int NPB = DQK == 256 ? 2 : 1;
+  static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes + NPB * P_BUF;
   static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
   static constexpr int NBAR = 2 * NS + 22;      // ..., QFREE, 4 per-producer fix-up barriers last
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
@@ -188,8 +191,12 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cl(uint32_t cbar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx_cl(uint32_t cbar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar), "r"(bytes)
+// An arrival with an expected byte count, without release semantics: it publishes no data of
+// its own (the TMA's byte count completes the phase), and a release arrive would first wait for
+// every earlier load of the thread, which in a producer loop means the next page-id lookup.
+__device__ __forceinline__ void mbar_expect_tx_cl_relaxed(uint32_t cbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar),
+               "r"(bytes)
                : "memory");
 }
 
@@ -376,7 +383,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sSlots = base + C::QS_BYTES;
-  const uint32_t sP = sSlots + NS * kSlotBytes;  // two P buffers
+  const uint32_t sP = sSlots + NS * kSlotBytes;  // NPB P buffers
   float* xl = reinterpret_cast<float*>(gbase + C::SMEM_DATA);  // [2 halves][128 rows]
   const uint32_t bars = base + C::SMEM_DATA + C::XL_BYTES;
   auto FULL = [&](int s) { return bars + 8u * s; };
@@ -448,8 +455,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (warp == 0 || warp == 10) {
     // ------------------------------------------------------------ producers
     // Each CTA loads its half of every tile: warp 0 the keys [32 rank, 32 rank + 32) of each K
-    // part, warp 10 the output columns [128 rank, 128 rank + 128) of each V tile, one box of BR
-    // key rows per lane, counted on the leader's FULL barrier. K lands as
+    // part, warp 10 the output columns [128 rank, 128 rank + 128) of each V tile, in boxes of BR
+    // key rows (one page each), counted on the leader's FULL barrier. K lands as
     // [key / 8][64-d chunk][8 rows][128 B] (a 4-D box), so every 8-key atom of QK's K-major
     // B operand sits 4096 bytes after the previous one across pages; V lands page-major as
     // [chunk][BR rows][128 B] (a 3-D box of two chunks), which PV's MN-major B operand reads with
@@ -468,9 +475,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int key_off = is_v ? 0 : (int)rank * kKH;      // this CTA's first key of a tile
     const uint32_t row_bytes = is_v ? 256u : 512u;       // bytes of one key row in a slot
     const int64_t head_rows = (int64_t)ps;
-    // lane i takes box i of the tile half (< nbox)
-    const int my_box = lane;
-    const bool box_lane = my_box < nbox;
     int32_t J = 0;  // tiles of this cluster's earlier units
     int32_t ui = 0;
     for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
@@ -492,7 +496,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (ui > 0 && !mbar_wait(QFREE, (ui - 1) & 1, abort_flag, a.status)) {
             go = 0;
           } else {
-            mbar_expect_tx_cl(LEAD(QFULL), u.ntok > 0 ? (uint32_t)C::QS_BYTES : 0u);
+            mbar_expect_tx_cl_relaxed(LEAD(QFULL), u.ntok > 0 ? (uint32_t)C::QS_BYTES : 0u);
             if (u.ntok > 0)
               for (int c = 0; c < (DQK - 256) / 64; ++c)
                 tma_load_3d(sQ + c * (kM * 128), &tm_q, 256 + c * 64, u.g * G, u.q0 + u.tok0,
@@ -504,85 +508,100 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           break;
         }
       }
-      auto page_of = [&](int32_t t) -> int32_t {  // raw page id of this lane's box (-1: past kv_len)
-        if (!box_lane) return -1;
-        const int32_t ks = u.kb0 + t * kBN + key_off + my_box * BR;
+      // Box coordinates are worked out a batch of TB tiles at a time, one box per lane: lane i
+      // holds box i mod nbox of tile (batch start + i / nbox). Page ids are read a batch ahead,
+      // so the per-tile path is a slot wait, one byte-count arrival and the copies.
+      const int TB = 32 / nbox;
+      const int my_t = lane / nbox, my_b = lane % nbox;
+      auto lookup = [&](int32_t t0) -> int32_t {  // page id of this lane's box in the batch at t0
+        const int32_t tt = t0 + my_t;
+        if (tt >= u.ntiles) return -1;
+        const int32_t ks = u.kb0 + tt * kBN + key_off + my_b * BR;
         if (ks >= u.kv_len) return -1;
         const int32_t lp = ks / ps;  // logical page; ring addressing wraps it over the pages held
         const int32_t pidx = u.kvp0 + (pl.ring ? lp % max(u.kvp1 - u.kvp0, 1) : lp);
         return (pidx < u.kvp1 && pidx < pl.num_page_ids) ? pl.page_ids[pidx] : a.num_pages;
       };
-      auto issue_part = [&](int s, int round, int c0, int32_t t, int32_t page) -> bool {
-        if (!__all_sync(0xffffffffu, mbar_wait(EMPTY(s), (round & 1) ^ 1, abort_flag, a.status)))
-          return false;
-        const int32_t kb = u.kb0 + t * kBN + key_off;  // first key of this CTA's half
-        const bool past = !box_lane || kb + my_box * BR >= u.kv_len;
-        const bool bad = !past && (page < 0 || page >= a.num_pages);
-        const bool any_bad = __any_sync(0xffffffffu, bad);
-        if (any_bad && lane == 0) atomicOr(a.status, kStatusBounds);
-        const bool load = !past && !bad;
-        // V rows past kv_len (partial last page) must read as zeros; K rows there are masked
-        const bool fix = any_bad || (is_v && __any_sync(0xffffffffu, box_lane && kb + my_box * BR + BR > u.kv_len));
-        const uint32_t box_bytes = (uint32_t)BR * row_bytes;
-        const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, load)) * box_bytes;
-        const uint32_t slot = sSlots + s * kSlotBytes;
-        const uint32_t bar = fix ? FIX : LEAD(FULL(s));
-        if (lane == 0) {
-          if (!fix) mbar_expect_tx_cl(bar, bytes);
-          else if (bytes > 0) mbar_expect_tx(FIX, bytes);
-        }
-        __syncwarp();
-        if (load) {
-          const int32_t row = (int32_t)((((int64_t)page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + u.g) *
-                                            head_rows + ((kb + my_box * BR) % ps));
-          if (is_v) {
-            tma_load_3d(slot + my_box * (BR * 256), &tm_v, 0, row, c0, bar);
-          } else {
-            tma_load_4d(slot + my_box * (BR * 512), &tm_kv, 0, 0, c0, row / 8, bar);
-          }
-        }
-        if (fix) {
-          if (bytes > 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(FIX, fix_phase, abort_flag, a.status))) return false;
-            fix_phase ^= 1u;
-          }
-          // zero this warp's rows that must not be read: keys past kv_len, keys on bad pages
-          for (int b = 0; b < nbox; ++b) {
-            const int32_t pb = __shfl_sync(0xffffffffu, page, b);
-            for (int r = 0; r < BR; ++r) {
-              const int32_t key = kb + b * BR + r;
-              if (key < u.kv_len && pb >= 0 && pb < a.num_pages) continue;
-              const int c = lane >> 3, w16 = lane & 7;  // chunk c, 16-byte piece w16 of a 128-B row
-              const int kt = b * BR + r;  // key within this CTA's half
-              if (is_v && c >= 2) continue;  // V rows are two chunks (256 B) here
-              const uint32_t off = is_v ? b * (BR * 256) + c * (BR * 128) + r * 128
-                                        : (kt >> 3) * 4096 + c * 1024 + (kt & 7) * 128;
-              *(reinterpret_cast<uint4*>(gbase + (slot - base) + off) + w16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cl(LEAD(FULL(s)));
-        }
-        return true;
-      };
-      // page ids are read two tiles ahead of the loads that use them
-      constexpr int kLook = 2;
-      int32_t qid[kLook + 1];
-#pragma unroll
-      for (int i = 0; i <= kLook; ++i) qid[i] = i < u.ntiles ? page_of(i) : -1;
+      int32_t pg_next = lookup(0);
+      int32_t my_page = -1, my_row = 0;
+      uint32_t bm_load = 0u, bm_fix = 0u;
+      const uint32_t box_mask = nbox >= 32 ? 0xffffffffu : ((1u << nbox) - 1u);
+      const uint32_t box_bytes = (uint32_t)BR * row_bytes;
       for (int32_t t = 0; ok && t < u.ntiles; ++t) {
-        const int32_t qn = t + kLook + 1 < u.ntiles ? page_of(t + kLook + 1) : -1;
         const int32_t JJ = J + t;
-        if (!is_v) {
-          for (int pp = 0; ok && pp < KP; ++pp)
-            ok = issue_part(KSLOT(JJ, pp), KROUND(JJ, pp), pp * 4, t, qid[0]);
-        } else {
-          ok = issue_part(VSLOT(JJ), (int)(JJ / NVR), u.dh * 4 + (int)rank * 2, t, qid[0]);
+        const int tb = t % TB;
+        if (tb == 0) {
+          my_page = pg_next;
+          pg_next = lookup(t + TB);  // used TB tiles from now
+          const int32_t tt = t + my_t;
+          const int32_t ks = u.kb0 + tt * kBN + key_off + my_b * BR;
+          const bool live = tt < u.ntiles;
+          const bool past = !live || ks >= u.kv_len;
+          const bool bad = !past && (my_page < 0 || my_page >= a.num_pages);
+          const bool load = !past && !bad;
+          // V rows past kv_len (partial last page) must read as zeros; K rows there are masked
+          const bool fixb = live && (bad || (is_v && ks + BR > u.kv_len));
+          bm_load = __ballot_sync(0xffffffffu, load);
+          bm_fix = __ballot_sync(0xffffffffu, fixb);
+          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, kStatusBounds);
+          my_row = load ? (int32_t)((((int64_t)my_page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + u.g) *
+                                        head_rows + (ks & (ps - 1)))
+                        : 0;
         }
-#pragma unroll
-        for (int i = 0; i < kLook; ++i) qid[i] = qid[i + 1];
-        qid[kLook] = qn;
+        const int sh = tb * nbox;
+        const bool fix = ((bm_fix >> sh) & box_mask) != 0u;
+        const uint32_t bytes = (uint32_t)__popc((bm_load >> sh) & box_mask) * box_bytes;
+        const bool issue = my_t == tb && ((bm_load >> lane) & 1u);
+        const int nparts = is_v ? 1 : KP;
+        for (int pp = 0; ok && pp < nparts; ++pp) {
+          const int s = is_v ? VSLOT(JJ) : KSLOT(JJ, pp);
+          const int round = is_v ? (int)(JJ / NVR) : KROUND(JJ, pp);
+          const int c0 = is_v ? u.dh * 4 + (int)rank * 2 : pp * 4;
+          int r = 1;
+          if (lane == 0) r = mbar_wait_inline(EMPTY(s), (round & 1) ^ 1, abort_flag, a.status) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, r, 0)) {
+            ok = false;
+            break;
+          }
+          const uint32_t slot = sSlots + s * kSlotBytes;
+          const uint32_t bar = fix ? FIX : LEAD(FULL(s));
+          if (lane == 0) {
+            if (!fix) mbar_expect_tx_cl_relaxed(bar, bytes);
+            else if (bytes > 0) mbar_expect_tx(FIX, bytes);
+          }
+          __syncwarp();
+          if (issue) {
+            if (is_v) tma_load_3d(slot + my_b * (BR * 256), &tm_v, 0, my_row, c0, bar);
+            else tma_load_4d(slot + my_b * (BR * 512), &tm_kv, 0, 0, c0, my_row / 8, bar);
+          }
+          if (fix) {
+            if (bytes > 0) {
+              if (!__all_sync(0xffffffffu, mbar_wait(FIX, fix_phase, abort_flag, a.status))) {
+                ok = false;
+                break;
+              }
+              fix_phase ^= 1u;
+            }
+            // zero this warp's rows that must not be read: keys past kv_len, keys on bad pages
+            const int32_t kb = u.kb0 + t * kBN + key_off;  // first key of this CTA's half
+            for (int b = 0; b < nbox; ++b) {
+              const int32_t pb = __shfl_sync(0xffffffffu, my_page, sh + b);
+              for (int rr = 0; rr < BR; ++rr) {
+                const int32_t key = kb + b * BR + rr;
+                if (key < u.kv_len && pb >= 0 && pb < a.num_pages) continue;
+                const int c = lane >> 3, w16 = lane & 7;  // chunk c, 16-byte piece w16 of a 128-B row
+                const int kt = b * BR + rr;  // key within this CTA's half
+                if (is_v && c >= 2) continue;  // V rows are two chunks (256 B) here
+                const uint32_t off = is_v ? b * (BR * 256) + c * (BR * 128) + rr * 128
+                                          : (kt >> 3) * 4096 + c * 1024 + (kt & 7) * 128;
+                *(reinterpret_cast<uint4*>(gbase + (slot - base) + off) + w16) = make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cl(LEAD(FULL(s)));
+          }
+        }
       }
       J += u.ntiles;
     }
@@ -671,7 +690,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t va = vs + (key / BR) * (BR * 256u) + (key % BR) * 128u;
             // P buffer: K-major, 128-byte swizzled rows of 64 keys; a K step is 32 bytes. The
             // unit's first MMA starts O afresh.
-            mma_ss<IDESC_PV>(tmem + kTmO, sdesc(sP + pb * C::P_BUF + kk * 32, 16, 1024),
+            mma_ss<IDESC_PV>(tmem + kTmO, sdesc(sP + (JJ % C::NPB) * C::P_BUF + kk * 32, 16, 1024),
                              sdesc(va, lbo, sbo), (jp > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(EMPTY(sidx));
@@ -823,12 +842,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
         }
         l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-        // P buffer b is free once PV(JJ - 2) has read it
-        if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ / NSB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+        // P buffer JJ mod NPB is free once PV(JJ - NPB) has read it
+        if (C::NPB == 2) {
+          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ / NSB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+        } else if (JJ > 0) {
+          const int32_t jp = JJ - 1;
+          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
+        }
         {
           // this row's 32 keys: four 16-byte chunks h*4 .. h*4+3 of its 128-byte row, at
           // positions swizzled by the row within its 8-row atom
-          unsigned char* prow_p = gbase + (sP - base) + b * C::P_BUF + (row >> 3) * 1024 + (row & 7) * 128;
+          unsigned char* prow_p = gbase + (sP - base) + (JJ % C::NPB) * C::P_BUF + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4*>(prow_p + (((h * 4 + c) ^ (row & 7)) << 4)) =
