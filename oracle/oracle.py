@@ -32,6 +32,12 @@ is ``[layer][page][K=0,V=1][kv_head][slot][D]``; key ``j`` is visible from
 query position ``p`` iff ``j <= p`` and (``window_left < 0`` or
 ``p - j <= window_left``).
 
+Cascade attention for requests sharing a key prefix is a variant the pages
+leave open; the oracle takes its plainest reading. A key segment is a request's
+run of key positions [kv_start, kv_start + n) held from slot 0 of its pages;
+``lse`` is the natural-log normaliser log sum_j exp(s_j) of the same masked
+softmax; ``merge_states`` combines the states of two disjoint key sets exactly.
+
 Row chunking in ``attention`` only bounds memory: every output row is the
 plain definition evaluated on its own.
 """
@@ -220,21 +226,56 @@ def gather_kv(pool_bits: np.ndarray, layer: int, pages_of_req, kv_len: int, page
     return k, v
 
 
-def attend_rows(q_rows, p_rows, k, v, window_left: int, sm_scale: float):
+def attend_rows(q_rows, p_rows, k, v, window_left: int, sm_scale: float, key_pos=None,
+                with_lse: bool = False):
     """Masked softmax attention of query rows q_rows [n, D] at positions p_rows
     over keys k [kv, D] and values v [kv, D]: o = sum_j softmax_j(s) v_j with
-    s_j = sm_scale * <q, k_j> over the visible j."""
+    s_j = sm_scale * <q, k_j> over the visible j. ``key_pos`` gives the keys'
+    positions (default 0 .. kv-1).
+
+    With ``with_lse`` also returns lse = log(sum_j exp(s_j)) over the visible j, the
+    normaliser of the same softmax (natural log). A row that sees no key has o = 0 and
+    lse = -inf: the neutral state of merge_states.
+    """
+    key_pos = np.arange(k.shape[0]) if key_pos is None else np.asarray(key_pos)
     s = sm_scale * (q_rows @ k.T)
-    mask = visible(np.asarray(p_rows)[:, None], np.arange(k.shape[0])[None, :], window_left)
+    mask = visible(np.asarray(p_rows)[:, None], key_pos[None, :], window_left)
     s = np.where(mask, s, -np.inf)
-    m = np.max(s, axis=1, keepdims=True)
+    seen = mask.any(axis=1)
+    m = np.where(seen, np.max(s, axis=1), 0.0)[:, None]
     e = np.where(mask, np.exp(s - m), 0.0)
-    return (e @ v) / np.sum(e, axis=1, keepdims=True)
+    den = np.sum(e, axis=1, keepdims=True)
+    o = np.where(seen[:, None], (e @ v) / np.where(den > 0, den, 1.0), 0.0)
+    if not with_lse:
+        return o
+    lse = np.where(seen, m[:, 0] + np.log(np.where(seen, den[:, 0], 1.0)), -np.inf)
+    return o, lse
+
+
+def merge_states(o_a, lse_a, o_b, lse_b):
+    """Attention state of the union of two disjoint key sets from the states of each:
+    with w_x = exp(lse_x - M), M = max(lse_a, lse_b), o = (w_a o_a + w_b o_b) / (w_a + w_b)
+    and lse = M + log(w_a + w_b). The softmax over the union is the two softmaxes reweighted
+    by their normalisers, so merging is exact; (0, -inf) is the neutral state.
+    """
+    o_a, o_b = np.asarray(o_a, np.float64), np.asarray(o_b, np.float64)
+    lse_a, lse_b = np.asarray(lse_a, np.float64), np.asarray(lse_b, np.float64)
+    M = np.maximum(lse_a, lse_b)
+    fin = np.isfinite(M)
+    Mz = np.where(fin, M, 0.0)
+    wa = np.where(np.isfinite(lse_a), np.exp(lse_a - Mz), 0.0)
+    wb = np.where(np.isfinite(lse_b), np.exp(lse_b - Mz), 0.0)
+    den = wa + wb
+    o = np.where(fin[..., None], (wa[..., None] * o_a + wb[..., None] * o_b)
+                 / np.where(den > 0, den, 1.0)[..., None], 0.0)
+    lse = np.where(fin, Mz + np.log(np.where(den > 0, den, 1.0)), -np.inf)
+    return o, lse
 
 
 def attention(q_bits, pool_bits, layer: int, qo_indptr, kv_page_indptr, page_ids,
               last_page_len, start_pos, num_kv_heads: int, window_left: int,
-              sm_scale: float, rows=None, row_chunk: int = 512, ring: bool = False):
+              sm_scale: float, rows=None, row_chunk: int = 512, ring: bool = False,
+              kv_start=None, return_lse: bool = False):
     """Paged prefill attention over a page table (fp64).
 
     q_bits: bf16 bits [T, Hq, D]; pool_bits: bf16 bits [L, P, 2, Hkv, ps, D].
@@ -243,6 +284,12 @@ def attention(q_bits, pool_bits, layer: int, qo_indptr, kv_page_indptr, page_ids
     queries sit at positions start_pos_r + t. Query head h reads KV head
     h // (Hq / Hkv). ``rows``: optional int array [n, 2] of (token, head) to
     evaluate; returns fp64 [n, D]. Without it returns fp64 [T, Hq, D].
+
+    ``kv_start`` (a key segment, for cascade attention): request r's pages hold key
+    positions [kv_start_r, kv_start_r + n_r), n_r = (pages_r - 1) * ps + last_page_len_r,
+    position kv_start_r + i in slot i (page i // ps, offset i % ps); keys outside the
+    segment are not seen. ``return_lse`` also returns the natural-log normaliser of every
+    row (see attend_rows), shaped like the output without its last axis.
     """
     qo_indptr = np.asarray(qo_indptr, dtype=np.int64)
     kv_page_indptr = np.asarray(kv_page_indptr, dtype=np.int64)
@@ -259,6 +306,7 @@ def attention(q_bits, pool_bits, layer: int, qo_indptr, kv_page_indptr, page_ids
     else:
         sel = np.asarray(rows, dtype=np.int64).reshape(-1, 2)
     out = np.zeros((len(sel), D), dtype=np.float64)
+    lse = np.full(len(sel), -np.inf, dtype=np.float64)
     sel_req = req_of[sel[:, 0]] if len(sel) else np.zeros(0, np.int64)
     for r in np.unique(sel_req):
         npages = kv_page_indptr[r + 1] - kv_page_indptr[r]
@@ -266,19 +314,23 @@ def attention(q_bits, pool_bits, layer: int, qo_indptr, kv_page_indptr, page_ids
             kv_len = int(np.asarray(start_pos, np.int64)[r] + qo_indptr[r + 1] - qo_indptr[r])
         else:
             kv_len = int((npages - 1) * ps + last_page_len[r])
+        # kv_len keys from slot 0 on: positions 0 .. kv_len-1, or the segment's
         k, v = gather_kv(pool_bits, layer, page_ids[kv_page_indptr[r]:kv_page_indptr[r + 1]],
                          kv_len, ps, ring)
+        key_pos = np.arange(kv_len, dtype=np.int64)
+        if kv_start is not None:
+            key_pos = key_pos + int(np.asarray(kv_start, np.int64)[r])
         idx_r = np.nonzero(sel_req == r)[0]
         for g in range(num_kv_heads):
             idx = idx_r[(sel[idx_r, 1] // group) == g]
             for c in range(0, len(idx), row_chunk):
                 ii = idx[c:c + row_chunk]
                 qr = bf16_to_f64(q_bits[sel[ii, 0], sel[ii, 1], :])
-                out[ii] = attend_rows(qr, pos_of[sel[ii, 0]], k[:, g, :], v[:, g, :],
-                                      window_left, sm_scale)
+                out[ii], lse[ii] = attend_rows(qr, pos_of[sel[ii, 0]], k[:, g, :], v[:, g, :],
+                                               window_left, sm_scale, key_pos, with_lse=True)
     if rows is None:
-        return out.reshape(T, Hq, D)
-    return out
+        out, lse = out.reshape(T, Hq, D), lse.reshape(T, Hq)
+    return (out, lse) if return_lse else out
 
 
 def visible_pairs(qo_indptr, start_pos, window_left: int) -> int:

@@ -232,3 +232,73 @@ def custom_family(fam: Family, qo_lens, start_pos, seed: int, num_pages: int | N
     if window_left is not None:
         fam = _with_window(fam, window_left)
     return family_inputs(rng, fam, b, num_layers, layer, pool_fill, seed + 1)
+
+
+@dataclass
+class CascadeInputs:
+    """Requests sharing a key prefix, in three page tables over one pool.
+
+    ``full`` holds each request's keys [0, L_r) in its own pages; ``prefix`` lists the
+    shared prefix pages (keys [0, prefix_len)) for every request; ``suffix`` holds each
+    request's keys [prefix_len, L_r) from slot 0 of its own pages. ``hist_k`` / ``hist_v``
+    are every request's key and value rows by position (bf16 bits [L_r, Hkv, D]; the prefix
+    rows are the same for every request). Filling the pool from them is left to the caller.
+    The queries are each request's last ``step_lens[r]`` positions.
+    """
+
+    q: np.ndarray                # uint16 bf16 bits [T, Hq, D]
+    hist_k: list
+    hist_v: list
+    full: Batch
+    prefix: Batch
+    suffix: Batch
+    prefix_len: int
+    num_kv_heads: int
+    head_dim: int
+
+
+def make_cascade(rng: np.random.Generator, prefix_len: int, suffix_lens, step_lens,
+                 page_size: int, num_qo_heads: int, num_kv_heads: int,
+                 head_dim: int) -> CascadeInputs:
+    suffix_lens = np.asarray(suffix_lens, np.int64)
+    step_lens = np.asarray(step_lens, np.int64)
+    if (step_lens > suffix_lens).any() or (step_lens < 1).any():
+        raise ValueError("each step must lie inside its request's own suffix")
+    R = len(suffix_lens)
+    L = prefix_len + suffix_lens
+    pre_k = bf16_normal(rng, (prefix_len, num_kv_heads, head_dim))
+    pre_v = bf16_normal(rng, (prefix_len, num_kv_heads, head_dim))
+    hist_k, hist_v = [], []
+    for r in range(R):
+        hist_k.append(np.concatenate([pre_k, bf16_normal(rng, (int(suffix_lens[r]), num_kv_heads, head_dim))]))
+        hist_v.append(np.concatenate([pre_v, bf16_normal(rng, (int(suffix_lens[r]), num_kv_heads, head_dim))]))
+    ceil = lambda n: -(-np.asarray(n, np.int64) // page_size)
+    n_pre = int(ceil(prefix_len))
+    n_suf = ceil(suffix_lens)
+    n_full = ceil(L)
+    total = n_pre + int(n_suf.sum()) + int(n_full.sum())
+    perm = rng.permutation(total).astype(np.int32)
+    pre_pages, off = perm[:n_pre], n_pre
+    suf_pages, full_pages = [], []
+    for r in range(R):
+        suf_pages.append(perm[off:off + n_suf[r]])
+        off += int(n_suf[r])
+    for r in range(R):
+        full_pages.append(perm[off:off + n_full[r]])
+        off += int(n_full[r])
+    qo = np.zeros(R + 1, np.int64)
+    qo[1:] = np.cumsum(step_lens)
+    start = (L - step_lens).astype(np.int64)
+
+    def table(pages, lens):
+        indptr = np.zeros(R + 1, np.int64)
+        indptr[1:] = np.cumsum([len(p) for p in pages])
+        lens = np.asarray(lens, np.int64)
+        last = (lens - (ceil(lens) - 1) * page_size).astype(np.int32)
+        return Batch(qo.copy(), indptr, np.concatenate(pages).astype(np.int32), last,
+                     start.copy(), page_size, total)
+
+    q = bf16_normal(rng, (int(qo[-1]), num_qo_heads, head_dim))
+    return CascadeInputs(q, hist_k, hist_v, table(full_pages, L),
+                         table([pre_pages] * R, [prefix_len] * R), table(suf_pages, suffix_lens),
+                         prefix_len, num_kv_heads, head_dim)

@@ -96,3 +96,31 @@ def slots_for_request(page_ids, kv_len, page_size):
             slot = 0
             pi += 1
     return out
+
+
+def lse_contiguous(q, k, q_positions, key_positions, window_left, sm_scale, group):
+    """log(sum_j exp(sm_scale <q, k_j>)) over the keys visible from each query, by loops.
+
+    q [n][Hq][D]; k [kv][Hkv][D] with key j at position key_positions[j]. Returns
+    lse [n][Hq]; -inf where a query sees no key.
+    """
+    out = []
+    for i, p in enumerate(q_positions):
+        row = []
+        for h in range(len(q[i])):
+            g = h // group
+            s = []
+            for j, kp in enumerate(key_positions):
+                if kp > p or (window_left >= 0 and p - kp > window_left):
+                    continue
+                acc = 0.0
+                for e in range(len(q[i][h])):
+                    acc += q[i][h][e] * k[j][g][e]
+                s.append(sm_scale * acc)
+            if not s:
+                row.append(-math.inf)
+                continue
+            mx = max(s)
+            row.append(mx + math.log(sum(math.exp(x - mx) for x in s)))
+        out.append(row)
+    return out

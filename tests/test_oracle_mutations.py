@@ -6,6 +6,7 @@ pin that should catch it; the test passes only if that pin now fails.
 import numpy as np
 import pytest
 
+import test_oracle_cascade as CA
 import test_oracle_pins as P
 from oracle import oracle as O
 
@@ -66,6 +67,30 @@ def _rotated_v_hd512(q_raw, k_raw, w_q, w_k, eps, positions, theta):
     return q, k, O.rope_half_split(k_raw * r_k, c, s)
 
 
+def _merge_without_normalisers(o_a, lse_a, o_b, lse_b):
+    # averages the two states as if both had the same normaliser
+    return (np.asarray(o_a) + np.asarray(o_b)) / 2, np.maximum(lse_a, lse_b)
+
+
+_attend = O.attend_rows
+
+
+def _lse_is_the_max(q_rows, p_rows, k, v, window_left, sm_scale, key_pos=None, with_lse=False):
+    # returns the row maximum where the log-sum-exp belongs
+    res = _attend(q_rows, p_rows, k, v, window_left, sm_scale, key_pos, with_lse)
+    if not with_lse:
+        return res
+    kp = np.arange(k.shape[0]) if key_pos is None else np.asarray(key_pos)
+    s = sm_scale * (q_rows @ k.T)
+    mask = O.visible(np.asarray(p_rows)[:, None], kp[None, :], window_left)
+    return res[0], np.where(mask.any(1), np.max(np.where(mask, s, -np.inf), axis=1), -np.inf)
+
+
+def _segment_ignored(q_rows, p_rows, k, v, window_left, sm_scale, key_pos=None, with_lse=False):
+    # reads a key segment as if it started at position 0
+    return _attend(q_rows, p_rows, k, v, window_left, sm_scale, None, with_lse)
+
+
 MUTATIONS = [
     ("rope_half_split", _interleaved_rope, lambda: P.test_rope_half_split_pairing_sign_and_frequency_d4()),
     ("rope_half_split", _sign_flipped_rope, lambda: P.test_rope_d2_is_textbook_rotation()),
@@ -75,6 +100,11 @@ MUTATIONS = [
     ("visible", _non_causal, lambda: P.test_attention_matches_brute(4, -1)),
     ("slot_of", _slot_off_by_one, lambda: P.test_slot_contract_matches_brute_walk()),
     ("prep_hd512", _rotated_v_hd512, lambda: P.test_prep_hd512_form_v_is_weightless_norm_of_raw_k()),
+    ("merge_states", _merge_without_normalisers,
+     lambda: CA.test_prefix_and_suffix_merge_to_the_single_pass(37, [5, 20, 1], [5, 3, 1], -1, 4)),
+    ("attend_rows", _lse_is_the_max, lambda: CA.test_lse_matches_brute_force()),
+    ("attend_rows", _segment_ignored,
+     lambda: CA.test_prefix_and_suffix_merge_to_the_single_pass(16, [9, 33], [9, 17], 11, 8)),
 ]
 
 
