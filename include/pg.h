@@ -143,6 +143,35 @@ int pg_plan_paged_prefill_ring(pg_plan_t* plan, int32_t num_req, const int64_t* 
                                int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                                int32_t window_left, pg_stream_t stream);
 
+/*
+ * pg_plan_paged_segment -- a plan over key segments, for cascade attention: requests that
+ * share a key prefix attend to it once as one segment and to their own keys as another,
+ * and pg_merge_attn_states combines the two results. (A variant the pages leave open:
+ * attention over a request's keys is the softmax of [P1] Description; splitting the keys
+ * into disjoint segments and merging by the softmax normalisers is exact.)
+ *
+ * Inputs as for pg_plan_paged_prefill, plus
+ *   kv_start[num_req]  int64 >= 0: request r's pages hold key positions
+ *                      [kv_start_r, kv_start_r + n_r), n_r = (pages_r - 1) * page_size
+ *                      + last_page_len_r, position kv_start_r + i in slot i (page
+ *                      i / page_size, offset i mod page_size) of its pages.
+ * Coverage: kv_start_r + n_r <= start_pos_r + qo_len_r (a segment holds no key past the
+ * step's last query; PG_ERR_COVERAGE otherwise). Queries see the keys of the segment
+ * that the causal and window rules allow: keys before kv_start_r are not part of this
+ * plan, and a query row that sees no key gets out = 0 and lse = -inf. Prep on a segment
+ * plan is accepted only when every request's step tokens are its segment's tail
+ * (kv_start_r <= start_pos_r and kv_start_r + n_r == start_pos_r + qo_len_r; prep calls
+ * fail with PG_ERR_COVERAGE otherwise); the pool pages may repeat across requests (a
+ * shared prefix lists the same pages for every request) as long as no prep writes them.
+ * Everything else (stream binding, in-place update, checks) is as for
+ * pg_plan_paged_prefill; kv_start == 0 for every request gives that plan.
+ */
+int pg_plan_paged_segment(pg_plan_t* plan, int32_t num_req, const int64_t* qo_indptr,
+                          const int64_t* kv_page_indptr, const int32_t* page_ids,
+                          const int32_t* last_page_len, const int64_t* kv_start,
+                          const int64_t* start_pos, int32_t num_qo_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t page_size, pg_stream_t stream);
+
 /* Free a plan (host and device storage; device frees are ordered on its stream). NULL is a no-op. */
 void pg_plan_destroy(pg_plan_t plan);
 
@@ -251,6 +280,40 @@ int pg_attn_paged_prefill_hd512(const pg_plan_t plan, const pg_pool_t* pool, int
                                 const pg_bf16_t* q, pg_bf16_t* out, int32_t window_left,
                                 float sm_scale, void* workspace, size_t ws_bytes,
                                 pg_stream_t stream);
+
+/*
+ * pg_attn_paged_prefill_lse / pg_attn_paged_prefill_hd512_lse -- the same attention,
+ * also writing each row's softmax normaliser
+ *   lse[t][h] = log( sum_j exp( sm_scale * <q[t][h], K_j> ) )   (natural log)
+ * over the keys the row sees, or -inf when it sees none (its out row is then 0).
+ *   lse [T][Hq] float32, 4-byte aligned, written (must not be NULL when T > 0:
+ *       PG_ERR_ARG)
+ * The kernels sum the bf16-rounded softmax weights they multiply V by, so lse agrees with
+ * out's normalisation. Every other argument, check and error as for the entries above.
+ */
+int pg_attn_paged_prefill_lse(const pg_plan_t plan, const pg_pool_t* pool, int32_t layer,
+                              const pg_bf16_t* q, pg_bf16_t* out, float* lse,
+                              int32_t window_left, float sm_scale, void* workspace,
+                              size_t ws_bytes, pg_stream_t stream);
+int pg_attn_paged_prefill_hd512_lse(const pg_plan_t plan, const pg_pool_t* pool, int32_t layer,
+                                    const pg_bf16_t* q, pg_bf16_t* out, float* lse,
+                                    int32_t window_left, float sm_scale, void* workspace,
+                                    size_t ws_bytes, pg_stream_t stream);
+
+/*
+ * pg_merge_attn_states -- combine two attention states over disjoint key sets, row by row:
+ * with w_x = exp(lse_x - M), M = max(lse_a, lse_b),
+ *   out = (w_a out_a + w_b out_b) / (w_a + w_b),   lse = M + log(w_a + w_b);
+ * a side with lse = -inf contributes nothing (both -inf: out = 0, lse = -inf).
+ *   out_a, out_b, out  [rows][head_dim] bf16, 16-byte aligned (out may alias either input)
+ *   lse_a, lse_b       [rows] float32; lse [rows] float32 or NULL (not written)
+ * head_dim > 0 and a multiple of 8; rows >= 0 (0 launches nothing), rows <= INT32_MAX.
+ * Errors: PG_ERR_ARG (null input, bad sizes), PG_ERR_ALIGN, PG_ERR_I32_OVERFLOW,
+ * PG_ERR_CUDA. Asynchronous on `stream`; no plan is involved.
+ */
+int pg_merge_attn_states(const pg_bf16_t* out_a, const float* lse_a, const pg_bf16_t* out_b,
+                         const float* lse_b, pg_bf16_t* out, float* lse, int64_t rows,
+                         int32_t head_dim, pg_stream_t stream);
 
 /* ---------------------------------------------------------------- decode without allocation */
 /*

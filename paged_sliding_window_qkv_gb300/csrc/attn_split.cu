@@ -27,6 +27,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
+constexpr float kLn2 = 0.69314718055994531f;  // log2 units to natural log
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -135,16 +136,19 @@ attn_split_kernel(AttnArgs a) {
   const int32_t kvp0 = pl.kv_page_indptr[r], kvp1 = pl.kv_page_indptr[r + 1];
   const int32_t ps = a.pool.page_size;
   const int32_t sp = pl.start_pos[r];
+  const int32_t ks0 = pl.kv_start[r];  // first key position held (a key segment's start)
   // ring addressing (window-crossing requests): every position below start + qo_len is held
-  const int32_t kv_len = pl.ring ? sp + qo_len : (kvp1 - kvp0 - 1) * ps + pl.last_page_len[r];
+  const int32_t kv_len =
+      pl.ring ? sp + qo_len : ks0 + (kvp1 - kvp0 - 1) * ps + pl.last_page_len[r];
   const int32_t p_first = sp + tok0, p_last = sp + tok0 + ntok - 1;
   const int32_t W = a.window_left;
-  int32_t lo = W >= 0 ? max(0, p_first - W) : 0;
+  int32_t lo = W >= 0 ? max(ks0, p_first - W) : ks0;
   int32_t hi = min(p_last + 1, kv_len);
   int32_t nchunks = 1;
   if (C::DECODE) {
     nchunks = (hi - lo + a.kv_chunk - 1) / a.kv_chunk;
-    if (chunk >= nchunks) return;
+    // a row that sees no key (possible in a key segment) is still written, by chunk 0
+    if (chunk >= max(nchunks, 1)) return;
     lo = lo + chunk * a.kv_chunk;
     hi = min(hi, lo + a.kv_chunk);
   }
@@ -174,14 +178,15 @@ attn_split_kernel(AttnArgs a) {
     bool valid = j < hi;
     const __nv_bfloat16* src = a.pool.layer_base;
     if (valid) {
-      const int32_t lp = j / ps;  // logical page; ring addressing wraps it over the pages held
+      const int32_t rel = j - ks0;  // index among the keys held
+      const int32_t lp = rel / ps;  // logical page; ring addressing wraps it over the pages held
       const int32_t pidx = kvp0 + (pl.ring ? lp % max(kvp1 - kvp0, 1) : lp);
       const int32_t page = pidx < kvp1 ? pl.page_ids[pidx] : -1;
       if (page < 0 || page >= a.pool.num_pages) {
         if (c0 == 0) atomicOr(a.status, kStatusBounds);
         valid = false;
       } else {
-        src = kv_base + (int64_t)page * a.pool.stride_page + (int64_t)(j % ps) * D;
+        src = kv_base + (int64_t)page * a.pool.stride_page + (int64_t)(rel % ps) * D;
       }
     }
 #pragma unroll
@@ -354,6 +359,11 @@ attn_split_kernel(AttnArgs a) {
 
   // ---- epilogue ----
   if (sm_sub == 0) sL[sm_row] = row_l;
+  if (a.lse && !(C::DECODE && nchunks > 1) && sm_sub == 0 && sm_valid) {
+    // natural-log normaliser of the row: row_m and row_l are in log2 units of the scores
+    a.lse[(int64_t)(q0 + tok0 + sm_tl) * Hq + g * G + (sm_row % G)] =
+        row_l > 0.f ? (row_m + log2f(row_l)) * kLn2 : -INFINITY;
+  }
   if (C::DECODE && nchunks > 1 && sm_sub == 0 && sm_valid) {
     const int h = g * G + (sm_row % G);
     float* ml = a.ws_ml + (((int64_t)r * Hq + h) * a.max_chunks + chunk) * 2;
@@ -397,10 +407,11 @@ attn_merge_kernel(AttnArgs a) {
   const PlanDev& pl = a.plan;
   const int32_t kvp0 = pl.kv_page_indptr[r], kvp1 = pl.kv_page_indptr[r + 1];
   const int32_t p = pl.start_pos[r];
+  const int32_t ks0 = pl.kv_start[r];
   const int32_t kv_len = pl.ring ? p + (pl.qo_indptr[r + 1] - pl.qo_indptr[r])
-                                 : (kvp1 - kvp0 - 1) * a.pool.page_size + pl.last_page_len[r];
+                                 : ks0 + (kvp1 - kvp0 - 1) * a.pool.page_size + pl.last_page_len[r];
   const int32_t W = a.window_left;
-  const int32_t lo = W >= 0 ? max(0, p - W) : 0;
+  const int32_t lo = W >= 0 ? max(ks0, p - W) : ks0;
   const int32_t hi = min(p + 1, kv_len);
   const int32_t nch = (hi - lo + a.kv_chunk - 1) / a.kv_chunk;
   if (nch <= 1) return;  // written directly by the partition kernel
@@ -418,6 +429,9 @@ attn_merge_kernel(AttnArgs a) {
     den += w;
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
+  if (a.lse && threadIdx.x == 0)
+    a.lse[(int64_t)pl.qo_indptr[r] * a.num_qo_heads + h] =
+        den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
   __nv_bfloat16* dst = a.out + ((int64_t)pl.qo_indptr[r] * a.num_qo_heads + h) * D + d;
   *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
   *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);

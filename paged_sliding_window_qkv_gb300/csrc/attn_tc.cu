@@ -104,6 +104,7 @@ struct TcArgs {
   int32_t num_qo_heads, group, cta_tile_q, window_left;
   int32_t page_size, num_pages, num_kv_heads, box_rows_k, box_rows_v;
   float scale_log2;
+  float* lse;  // optional [T][Hq] natural-log normaliser of each row (null: not written)
   int* status;
 };
 
@@ -333,7 +334,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // order, so the last pairs come first); cluster i takes one unit per round of clusters.
 struct TcUnit {
   int32_t q0, tok0, ntok;  // this CTA's query tile: request's first token, tile start, tokens (0: none)
-  int32_t kvp0, kvp1, kv_len, sp, kb0, ntiles, g, dh;
+  // keys held: positions [kv_start, kv_len); key tiles start kb0 + 64 t, 64-aligned from kv_start
+  int32_t kvp0, kvp1, kv_len, kv_start, sp, kb0, ntiles, g, dh;
 };
 __device__ __forceinline__ TcUnit tc_unit(const TcArgs& a, int32_t w, int32_t ndh, int32_t rank) {
   const PlanDev& pl = a.plan;
@@ -353,12 +355,14 @@ __device__ __forceinline__ TcUnit tc_unit(const TcArgs& a, int32_t w, int32_t nd
   u.kvp0 = e1.x;
   u.kvp1 = e1.y;
   u.kv_len = e1.z;
+  u.kv_start = e1.w;
   // the pair's key range: the keys some row of either tile sees
   const int32_t W = a.window_left;
   const int32_t p_first = u.sp + t0, p_last = u.sp + min(t0 + 2 * TQ, len) - 1;
-  const int32_t lo = W >= 0 ? max(0, p_first - W) : 0;
+  const int32_t lo = W >= 0 ? max(u.kv_start, p_first - W) : u.kv_start;
   const int32_t hi = min(p_last + 1, u.kv_len);
-  u.kb0 = lo & ~(kBN - 1);
+  // tiles are aligned from the first key held, so a box of page rows never straddles a page
+  u.kb0 = u.kv_start + ((lo - u.kv_start) & ~(kBN - 1));
   u.ntiles = hi > u.kb0 ? (hi - u.kb0 + kBN - 1) / kBN : 0;
   return u;
 }
@@ -518,7 +522,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (tt >= u.ntiles) return -1;
         const int32_t ks = u.kb0 + tt * kBN + key_off + my_b * BR;
         if (ks >= u.kv_len) return -1;
-        const int32_t lp = ks / ps;  // logical page; ring addressing wraps it over the pages held
+        const int32_t lp = (ks - u.kv_start) / ps;  // logical page; a ring wraps it over its pages
         const int32_t pidx = u.kvp0 + (pl.ring ? lp % max(u.kvp1 - u.kvp0, 1) : lp);
         return (pidx < u.kvp1 && pidx < pl.num_page_ids) ? pl.page_ids[pidx] : a.num_pages;
       };
@@ -545,7 +549,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           bm_fix = __ballot_sync(0xffffffffu, fixb);
           if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, kStatusBounds);
           my_row = load ? (int32_t)((((int64_t)my_page * 2 + (is_v ? 1 : 0)) * a.num_kv_heads + u.g) *
-                                        head_rows + (ks & (ps - 1)))
+                                        head_rows + ((ks - u.kv_start) & (ps - 1)))
                         : 0;
         }
         const int sh = tb * nbox;
@@ -756,7 +760,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int32_t ntiles = u.ntiles;
       const bool rvalid = row < u.ntok * G;
       const int32_t prow = u.sp + u.tok0 + row / G;
-      const int32_t rlo = W >= 0 ? max(0, prow - W) : 0;
+      const int32_t rlo = W >= 0 ? max(u.kv_start, prow - W) : u.kv_start;
       const int32_t rhi = min(prow + 1, u.kv_len);
       float m_ref = -INFINITY, l = 0.f;
       for (int32_t j = 0; ok && j < ntiles; ++j) {
@@ -892,6 +896,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // bytes of the row)
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (a.lse && rvalid && h == 0 && u.dh == 0)  // both output halves of hd512 agree
+          a.lse[(int64_t)(u.q0 + u.tok0 + row / G) * Hq + u.g * G + row % G] =
+              l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
         __nv_bfloat16* dst = a.out + ((int64_t)(u.q0 + u.tok0 + row / G) * Hq + u.g * G + row % G) * DQK +
                              u.dh * kDV + h * (kDV / 2);
         for (int c2 = 0; c2 < kDV / 64; c2 += 2) {
@@ -1030,6 +1037,7 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   t.stride_kv = a.pool.stride_kv;
   t.stride_head = a.pool.stride_head;
   t.scale_log2 = a.sm_scale_log2;
+  t.lse = a.lse;
   t.status = a.status;
 
   static int sms[128] = {0};  // the shared-memory opt-in and the SM count, per device

@@ -71,12 +71,15 @@ struct pg_plan {
   int32_t cta_tile_q = 0, decode = 0, kv_chunk = 0, max_chunks = 0, num_work = 0, num_pairs = 0;
   int32_t num_page_ids = 0;
   int32_t ring = 0, ring_window = -1;  // ring addressing (window-crossing requests) and its window
+  // key segments (cascade attention): request r's pages hold key positions
+  // [kv_start_r, kv_start_r + n_r); prep_ok: every request's step tokens are its segment's tail
+  int32_t segment = 0, prep_ok = 1;
   cudaStream_t stream = nullptr;
   int device = 0;
   int32_t* dev = nullptr;  // one device allocation holding every metadata array
   size_t dev_elems = 0;
   // offsets (elements) of each array inside `dev`
-  size_t o_qo = 0, o_kvp = 0, o_pages = 0, o_last = 0, o_start = 0, o_tokreq = 0,
+  size_t o_qo = 0, o_kvp = 0, o_pages = 0, o_last = 0, o_start = 0, o_kvs = 0, o_tokreq = 0,
          o_wreq = 0, o_wtok = 0, o_pair = 0;
 };
 
@@ -88,12 +91,17 @@ namespace {
 // last_page_len is not read, and the ring must hold the window plus the step
 // (pages * ps >= ring_window + qo_len), so no key a query of the step can see is overwritten by
 // the step's own writes.
+// kv_start != null: key segments (linear addressing within the segment): request r's pages hold
+// key positions [kv_start_r, kv_start_r + n_r), n_r = (pages - 1) * ps + last_page_len_r, from
+// slot 0 on; the segment ends at or before the step's last position.
 int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
                const int64_t* kv_page_indptr, const int32_t* page_ids,
                const int32_t* last_page_len, const int64_t* start_pos, int32_t Hq,
                int32_t Hkv, int32_t D, int32_t ps, cudaStream_t stream,
-               int32_t ring_window = -1) {
+               int32_t ring_window = -1, const int64_t* kv_start = nullptr) {
   const bool ring = ring_window >= 0;
+  const bool segment = kv_start != nullptr;
+  if (ring && segment) return PG_ERR_ARG;
   // The head relation is settled before anything divides by num_kv_heads.
   if (Hkv == 0) return PG_ERR_ZERO_KV_HEADS;
   if (Hkv < 0 || Hq <= 0 || Hq % Hkv != 0) return PG_ERR_HEADS;
@@ -104,12 +112,13 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
     return PG_ERR_ARG;
   const int32_t group = Hq / Hkv;
 
-  std::vector<int32_t> qo(num_req + 1, 0), kvp(num_req + 1, 0), last(num_req), start(num_req);
+  std::vector<int32_t> qo(num_req + 1, 0), kvp(num_req + 1, 0), last(num_req), start(num_req),
+      kvs(num_req, 0);
   if (num_req > 0) {
     if (qo_indptr[0] != 0 || kv_page_indptr[0] != 0) return PG_ERR_ARG;
   }
-  int32_t max_page = -1, max_last = 0, max_qo = 0, max_kv = 0, max_end = 0;
-  bool all_one = num_req > 0;
+  int32_t max_page = -1, max_last = 0, max_qo = 0, max_kv = 0, max_end = 0, max_seen = 0;
+  bool all_one = num_req > 0, prep_ok = true;
   for (int32_t r = 0; r < num_req; ++r) {
     const int64_t q0 = qo_indptr[r], q1 = qo_indptr[r + 1];
     const int64_t k0 = kv_page_indptr[r], k1 = kv_page_indptr[r + 1];
@@ -121,14 +130,22 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
     int64_t pos_end = 0;
     if (!add_i64(sp, qo_len, &pos_end) || !fits_i32(pos_end)) return PG_ERR_I32_OVERFLOW;
     int32_t lpl = 0;
-    int64_t kv_len = 0;
+    int64_t kv_len = 0, seg0 = 0;  // kv_len: end of the keys held (exclusive); seg0: first
     if (!ring) {
       lpl = last_page_len[r];
       if (lpl < 1 || lpl > ps) return PG_ERR_LAST_PAGE_LEN;
       if (!mul_i64(k1 - k0 - 1, ps, &kv_len) || !add_i64(kv_len, lpl, &kv_len))
         return PG_ERR_I32_OVERFLOW;
+      if (segment) {
+        seg0 = kv_start[r];
+        if (seg0 < 0) return PG_ERR_ARG;
+        if (!add_i64(seg0, kv_len, &kv_len)) return PG_ERR_I32_OVERFLOW;
+      }
       if (!fits_i32(kv_len)) return PG_ERR_I32_OVERFLOW;
-      if (kv_len != pos_end) return PG_ERR_COVERAGE;
+      if (!segment && kv_len != pos_end) return PG_ERR_COVERAGE;
+      // a segment holds no key past the step's last position (no query could see it)
+      if (segment && kv_len > pos_end) return PG_ERR_COVERAGE;
+      if (segment && !(kv_len == pos_end && sp >= seg0)) prep_ok = false;
     } else {
       int64_t cap = 0, need = 0;
       if (!mul_i64(k1 - k0, ps, &cap) || !add_i64(ring_window, qo_len, &need))
@@ -142,6 +159,8 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
     kvp[r + 1] = (int32_t)k1;
     last[r] = lpl;
     start[r] = (int32_t)sp;
+    kvs[r] = (int32_t)seg0;
+    if (kv_len - seg0 > max_seen) max_seen = (int32_t)(kv_len - seg0);
     if (lpl > max_last) max_last = lpl;
     if (qo_len > max_qo) max_qo = (int32_t)qo_len;
     if (kv_len > max_kv) max_kv = (int32_t)kv_len;
@@ -170,8 +189,9 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
       // the tcgen05 prefill runs query tiles in pairs (one per CTA of a cluster) that share
       // their key tiles; a request with an odd number of tiles ends with a single-tile pair
       for (int64_t t = 0; t < len; t += 2 * (int64_t)cta) {
-        const int32_t kv_len = ring ? start[r] + len : (kvp[r + 1] - kvp[r] - 1) * ps + last[r];
-        const int32_t e[8] = {(int32_t)t, qo[r], len, start[r], kvp[r], kvp[r + 1], kv_len, r};
+        const int32_t kv_len =
+            ring ? start[r] + len : kvs[r] + (kvp[r + 1] - kvp[r] - 1) * ps + last[r];
+        const int32_t e[8] = {(int32_t)t, qo[r], len, start[r], kvp[r], kvp[r + 1], kv_len, kvs[r]};
         ptab.insert(ptab.end(), e, e + 8);
       }
     }
@@ -198,6 +218,7 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   q.o_pages = put(pids.data(), pids.size());
   q.o_last = put(last.data(), last.size());
   q.o_start = put(start.data(), start.size());
+  q.o_kvs = put(kvs.data(), kvs.size());
   q.o_tokreq = put(tokreq.data(), tokreq.size());
   q.o_wreq = put(wreq.data(), wreq.size());
   q.o_wtok = put(wtok.data(), wtok.size());
@@ -223,10 +244,12 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   q.max_kv_len = max_kv; q.max_pos_end = max_end;
   q.cta_tile_q = cta; q.decode = all_one ? 1 : 0; q.kv_chunk = chunk;
   // decode partials: a query sees at most window + 1 keys in ring addressing
-  const int64_t seen = ring ? std::min<int64_t>(max_kv, (int64_t)ring_window + 1) : max_kv;
+  const int64_t seen = ring ? std::min<int64_t>(max_kv, (int64_t)ring_window + 1) : max_seen;
   q.max_chunks = seen > 0 ? (int32_t)((seen + chunk - 1) / chunk) : 0;
   q.ring = ring ? 1 : 0;
   q.ring_window = ring ? ring_window : -1;
+  q.segment = segment ? 1 : 0;
+  q.prep_ok = prep_ok ? 1 : 0;
   q.num_work = (int32_t)nwork; q.num_pairs = (int32_t)(ptab.size() / 8); q.num_page_ids = NP;
   q.stream = stream; q.device = dev;
   q.dev = d; q.dev_elems = host.size();
@@ -245,6 +268,7 @@ PlanDev plan_dev(const pg_plan* p) {
   v.page_ids = p->dev + p->o_pages;
   v.last_page_len = p->dev + p->o_last;
   v.start_pos = p->dev + p->o_start;
+  v.kv_start = p->dev + p->o_kvs;
   v.tok_req = p->dev + p->o_tokreq;
   v.work_req = p->dev + p->o_wreq;
   v.work_tok0 = p->dev + p->o_wtok;
@@ -320,6 +344,8 @@ int prep_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
                 pg_bf16_t* q_out, cudaStream_t stream, PrepArgs* a) {
   if (!plan) return PG_ERR_ARG;
   if (stream != plan->stream) return PG_ERR_STREAM;
+  // a key-segment plan takes prep only when every step's tokens are its segment's tail
+  if (plan->segment && !plan->prep_ok) return PG_ERR_COVERAGE;
   int rc_ = check_plan_pool(plan, pool, layer, D);
   if (rc_) return rc_;
   if (!std::isfinite(eps) || !(eps > 0.0f)) return PG_ERR_NONFINITE;
@@ -362,8 +388,8 @@ size_t workspace_bytes(const pg_plan* p) {
 }
 
 int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32_t D,
-                const pg_bf16_t* q, pg_bf16_t* out, int32_t window_left, float sm_scale,
-                void* ws, size_t ws_bytes, cudaStream_t stream) {
+                const pg_bf16_t* q, pg_bf16_t* out, float* lse, int32_t window_left,
+                float sm_scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!plan) return PG_ERR_ARG;
   if (stream != plan->stream) return PG_ERR_STREAM;
   int rc = check_plan_pool(plan, pool, layer, D);
@@ -382,6 +408,7 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
   if (plan->num_tokens == 0) return PG_OK;
   if (!q || !out) return PG_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return PG_ERR_ALIGN;
+  if (lse && ((uintptr_t)lse & 3u) != 0) return PG_ERR_ALIGN;
   const size_t need = workspace_bytes(plan);
   if (need > 0) {
     if (!ws || ws_bytes < need) return PG_ERR_WORKSPACE;
@@ -395,6 +422,7 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
   a.pool = pool_dev(pool, layer);
   a.q = reinterpret_cast<const __nv_bfloat16*>(q);
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
   a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   a.window_left = window_left;
   a.num_qo_heads = plan->num_qo_heads;
@@ -482,6 +510,33 @@ int pg_plan_paged_prefill_ring(pg_plan_t* plan, int32_t num_req, const int64_t* 
   return PG_OK;
 }
 
+int pg_plan_paged_segment(pg_plan_t* plan, int32_t num_req, const int64_t* qo_indptr,
+                          const int64_t* kv_page_indptr, const int32_t* page_ids,
+                          const int32_t* last_page_len, const int64_t* kv_start,
+                          const int64_t* start_pos, int32_t num_qo_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t page_size, pg_stream_t stream) {
+  if (!plan) return PG_ERR_ARG;
+  if (num_req > 0 && !kv_start) return PG_ERR_ARG;
+  static const int64_t kNoSegments = 0;  // a non-null pointer for an empty batch
+  const int64_t* ks = kv_start ? kv_start : &kNoSegments;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (*plan) {
+    if ((*plan)->stream != s) return PG_ERR_STREAM;
+    return build_plan(*plan, num_req, qo_indptr, kv_page_indptr, page_ids, last_page_len,
+                      start_pos, num_qo_heads, num_kv_heads, head_dim, page_size, s, -1, ks);
+  }
+  pg_plan* p = new (std::nothrow) pg_plan();
+  if (!p) return PG_ERR_ARG;
+  int rc = build_plan(p, num_req, qo_indptr, kv_page_indptr, page_ids, last_page_len, start_pos,
+                      num_qo_heads, num_kv_heads, head_dim, page_size, s, -1, ks);
+  if (rc != PG_OK) {
+    delete p;
+    return rc;
+  }
+  *plan = p;
+  return PG_OK;
+}
+
 void pg_plan_destroy(pg_plan_t plan) {
   if (!plan) return;
   if (plan->dev) cudaFreeAsync(plan->dev, plan->stream);
@@ -546,7 +601,7 @@ size_t pg_workspace_bytes(const pg_plan_t plan) { return workspace_bytes(plan); 
 int pg_attn_paged_prefill(const pg_plan_t plan, const pg_pool_t* pool, int32_t layer,
                           const pg_bf16_t* q, pg_bf16_t* out, int32_t window_left, float sm_scale,
                           void* workspace, size_t ws_bytes, pg_stream_t stream) {
-  return attn_common(plan, pool, layer, 256, q, out, window_left, sm_scale, workspace, ws_bytes,
+  return attn_common(plan, pool, layer, 256, q, out, nullptr, window_left, sm_scale, workspace, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -554,8 +609,44 @@ int pg_attn_paged_prefill_hd512(const pg_plan_t plan, const pg_pool_t* pool, int
                                 const pg_bf16_t* q, pg_bf16_t* out, int32_t window_left,
                                 float sm_scale, void* workspace, size_t ws_bytes,
                                 pg_stream_t stream) {
-  return attn_common(plan, pool, layer, 512, q, out, window_left, sm_scale, workspace, ws_bytes,
+  return attn_common(plan, pool, layer, 512, q, out, nullptr, window_left, sm_scale, workspace, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pg_attn_paged_prefill_lse(const pg_plan_t plan, const pg_pool_t* pool, int32_t layer,
+                              const pg_bf16_t* q, pg_bf16_t* out, float* lse,
+                              int32_t window_left, float sm_scale, void* workspace,
+                              size_t ws_bytes, pg_stream_t stream) {
+  if (!lse && plan && plan->num_tokens > 0) return PG_ERR_ARG;
+  return attn_common(plan, pool, layer, 256, q, out, lse, window_left, sm_scale, workspace,
+                     ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pg_attn_paged_prefill_hd512_lse(const pg_plan_t plan, const pg_pool_t* pool, int32_t layer,
+                                    const pg_bf16_t* q, pg_bf16_t* out, float* lse,
+                                    int32_t window_left, float sm_scale, void* workspace,
+                                    size_t ws_bytes, pg_stream_t stream) {
+  if (!lse && plan && plan->num_tokens > 0) return PG_ERR_ARG;
+  return attn_common(plan, pool, layer, 512, q, out, lse, window_left, sm_scale, workspace,
+                     ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pg_merge_attn_states(const pg_bf16_t* out_a, const float* lse_a, const pg_bf16_t* out_b,
+                         const float* lse_b, pg_bf16_t* out, float* lse, int64_t rows,
+                         int32_t head_dim, pg_stream_t stream) {
+  if (rows < 0 || head_dim <= 0 || head_dim % 8 != 0) return PG_ERR_ARG;
+  if (rows > INT32_MAX) return PG_ERR_I32_OVERFLOW;
+  if (rows == 0) return PG_OK;
+  if (!out_a || !lse_a || !out_b || !lse_b || !out) return PG_ERR_ARG;
+  if (!aligned16(out_a) || !aligned16(out_b) || !aligned16(out)) return PG_ERR_ALIGN;
+  if (((uintptr_t)lse_a & 3u) || ((uintptr_t)lse_b & 3u) || ((uintptr_t)lse & 3u))
+    return PG_ERR_ALIGN;
+  const cudaError_t e = launch_merge_states(
+      reinterpret_cast<const __nv_bfloat16*>(out_a), lse_a,
+      reinterpret_cast<const __nv_bfloat16*>(out_b), lse_b,
+      reinterpret_cast<__nv_bfloat16*>(out), lse, (int32_t)rows, head_dim,
+      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PG_OK : PG_ERR_CUDA;
 }
 
 int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, int32_t layer,
@@ -578,6 +669,7 @@ int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, in
   if (kernel_cta == 0 || kernel_cta != plan->cta_tile_q) return PG_ERR_PLAN_MISMATCH;
   if (attn_kernel_kv_chunk(D) != plan->kv_chunk) return PG_ERR_PLAN_MISMATCH;
   if (window_left < -1) return PG_ERR_WINDOW;
+  if (plan->ring && (window_left < 0 || window_left > plan->ring_window)) return PG_ERR_WINDOW;
   if (!std::isfinite(sm_scale)) return PG_ERR_NONFINITE;
   if (plan->num_tokens == 0) return PG_OK;
   if (!q || !out) return PG_ERR_ARG;
@@ -590,6 +682,7 @@ int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, in
   a.pool = pool_dev(pool, layer);
   a.q = reinterpret_cast<const __nv_bfloat16*>(q);
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.lse = nullptr;
   a.ws_o = nullptr;
   a.ws_ml = nullptr;
   a.sm_scale_log2 = sm_scale * 1.4426950408889634f;

@@ -14,12 +14,14 @@ struct PlanDev {
   const int32_t* page_ids;        // [num_page_ids]
   const int32_t* last_page_len;   // [R]
   const int32_t* start_pos;       // [R]
+  const int32_t* kv_start;        // [R]   first key position held (0 unless a key segment)
   const int32_t* tok_req;         // [T]   request of each token row
   const int32_t* work_req;        // [num_work] prefill work item: request
   const int32_t* work_tok0;       // [num_work] prefill work item: first request-local token
   // [num_pairs][8]: two consecutive query tiles of one request, with the request's geometry so
   // a kernel reads it in one step: {first request-local token of the pair, qo_indptr[r],
-  // qo_len, start_pos, kv_page_indptr[r], kv_page_indptr[r + 1], kv_len, r}
+  // qo_len, start_pos, kv_page_indptr[r], kv_page_indptr[r + 1], kv_end, kv_start}; the keys
+  // held are positions [kv_start, kv_end)
   const int32_t* pair_tab;
   int32_t num_req, num_tokens, num_page_ids, num_work, num_pairs;
   // ring addressing: logical page pos / page_size of request r is its page
@@ -57,6 +59,7 @@ struct AttnArgs {
   PoolDev pool;
   const __nv_bfloat16* q;
   __nv_bfloat16* out;
+  float* lse;     // optional [T][Hq] natural-log normaliser of each row (null: not written)
   float* ws_o;    // decode form: partial outputs [R][Hq][max_chunks][D]
   float* ws_ml;   // decode form: [R][Hq][max_chunks][2] (running max in log2 units, sum)
   float sm_scale_log2;  // sm_scale * log2(e)
@@ -98,5 +101,11 @@ cudaError_t launch_attn_decode(const AttnArgs& a, int32_t head_dim, cudaStream_t
 // Decode attention with its partials in the library's static scratch (no allocation).
 // The caller has already checked the plan's workspace size against that scratch.
 cudaError_t launch_attn_decode_static(AttnArgs a, int32_t head_dim, cudaStream_t stream);
+
+// Merge of two attention states over disjoint key sets (cascade attention), row by row.
+cudaError_t launch_merge_states(const __nv_bfloat16* out_a, const float* lse_a,
+                                const __nv_bfloat16* out_b, const float* lse_b,
+                                __nv_bfloat16* out, float* lse, int32_t rows, int32_t head_dim,
+                                cudaStream_t stream);
 
 }  // namespace pg

@@ -127,13 +127,16 @@ __device__ __forceinline__ bool token_meta(const PrepArgs& a, int32_t t, TokMeta
   const int32_t kvp0 = pl.kv_page_indptr[r], npg = pl.kv_page_indptr[r + 1] - kvp0;
   if (t < q0 || t >= pl.qo_indptr[r + 1] || pos < 0 || pos >= a.rope_rows || npg <= 0)
     return false;
-  // ring addressing: logical page pos / ps lives in page (pos / ps) mod (pages held)
-  const int32_t pidx = kvp0 + (pl.ring ? (pos / ps) % npg : pos / ps);
+  // the position's index among the keys the request holds (a key segment starts at kv_start)
+  const int32_t rel = pos - pl.kv_start[r];
+  if (rel < 0) return false;
+  // ring addressing: logical page rel / ps lives in page (rel / ps) mod (pages held)
+  const int32_t pidx = kvp0 + (pl.ring ? (rel / ps) % npg : rel / ps);
   if (pidx >= kvp0 + npg || pidx >= pl.num_page_ids) return false;
   const int32_t page = pl.page_ids[pidx];
   if (page < 0 || page >= a.pool.num_pages) return false;
   m->pos = pos;
-  m->slot = (int64_t)page * a.pool.stride_page + (int64_t)(pos % ps) * a.pool.head_dim;
+  m->slot = (int64_t)page * a.pool.stride_page + (int64_t)(rel % ps) * a.pool.head_dim;
   m->ok = 1;
   return true;
 }

@@ -85,6 +85,8 @@ _plan = _sig("pg_plan_paged_prefill", C.c_int, C.POINTER(_P), _I32, _P, _P, _P, 
              _I32, _I32, _I32, _I32, _P)
 _plan_ring = _sig("pg_plan_paged_prefill_ring", C.c_int, C.POINTER(_P), _I32, _P, _P, _P, _P,
                   _I32, _I32, _I32, _I32, _I32, _P)
+_plan_seg = _sig("pg_plan_paged_segment", C.c_int, C.POINTER(_P), _I32, _P, _P, _P, _P, _P, _P,
+                 _I32, _I32, _I32, _I32, _P)
 _destroy = _sig("pg_plan_destroy", None, _P)
 _info = _sig("pg_plan_info", C.c_int, _P, C.POINTER(pg_plan_info_t))
 _rope = _sig("pg_rope_table", C.c_int, _P, _P, _I32, _I32, _F64, _P)
@@ -208,6 +210,23 @@ def pg_plan_paged_prefill_ring(plan, num_req, qo_indptr, kv_page_indptr, page_id
     return rc, (Plan(h.value) if rc == PG_OK else None)
 
 
+def pg_plan_paged_segment(plan, num_req, qo_indptr, kv_page_indptr, page_ids, last_page_len,
+                          kv_start, start_pos, num_qo_heads, num_kv_heads, head_dim, page_size,
+                          stream=None):
+    """Build (plan=None) or update (plan=Plan) a key-segment plan. Returns (status, Plan or
+    None)."""
+    h = _P(plan.handle if plan is not None else None)
+    keep = [_host(qo_indptr, np.int64), _host(kv_page_indptr, np.int64),
+            _host(page_ids, np.int32), _host(last_page_len, np.int32),
+            _host(kv_start, np.int64), _host(start_pos, np.int64)]
+    rc = _plan_seg(C.byref(h), int(num_req), *[k[1] for k in keep], int(num_qo_heads),
+                   int(num_kv_heads), int(head_dim), int(page_size), _stream(stream))
+    del keep
+    if plan is not None:
+        return rc, plan
+    return rc, (Plan(h.value) if rc == PG_OK else None)
+
+
 def pg_workspace_bytes(plan) -> int:
     return int(_wsb(plan.handle if plan is not None else None))
 
@@ -263,6 +282,33 @@ def pg_attn_paged_prefill_hd512(plan, pool: pg_pool_t, layer, q, out, window_lef
                     _stream(stream))
 
 
+_attn256_lse = _sig("pg_attn_paged_prefill_lse", C.c_int, _P, C.POINTER(pg_pool_t), _I32, _P, _P,
+                    _P, _I32, _F32, _P, C.c_size_t, _P)
+_attn512_lse = _sig("pg_attn_paged_prefill_hd512_lse", C.c_int, _P, C.POINTER(pg_pool_t), _I32, _P,
+                    _P, _P, _I32, _F32, _P, C.c_size_t, _P)
+_merge = _sig("pg_merge_attn_states", C.c_int, _P, _P, _P, _P, _P, _P, _I64, _I32, _P)
+
+
+def pg_attn_paged_prefill_lse(plan, pool: pg_pool_t, layer, q, out, lse, window_left, sm_scale,
+                              workspace=None, ws_bytes=0, stream=None) -> int:
+    return _attn256_lse(plan.handle if plan is not None else None, C.byref(pool), int(layer),
+                        _ptr(q), _ptr(out), _ptr(lse), int(window_left), float(sm_scale),
+                        _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def pg_attn_paged_prefill_hd512_lse(plan, pool: pg_pool_t, layer, q, out, lse, window_left,
+                                    sm_scale, workspace=None, ws_bytes=0, stream=None) -> int:
+    return _attn512_lse(plan.handle if plan is not None else None, C.byref(pool), int(layer),
+                        _ptr(q), _ptr(out), _ptr(lse), int(window_left), float(sm_scale),
+                        _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def pg_merge_attn_states(out_a, lse_a, out_b, lse_b, out, lse, rows, head_dim,
+                         stream=None) -> int:
+    return _merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out), _ptr(lse),
+                  int(rows), int(head_dim), _stream(stream))
+
+
 def pg_attn_paged_decode_noalloc(plan, pool: pg_pool_t, layer, q, out, window_left, sm_scale,
                                  stream=None) -> int:
     """Decode attention with the library's static scratch; allocates nothing."""
@@ -270,7 +316,9 @@ def pg_attn_paged_decode_noalloc(plan, pool: pg_pool_t, layer, q, out, window_le
                          _ptr(q), _ptr(out), int(window_left), float(sm_scale), _stream(stream))
 
 
-EXPORTED = ["pg_plan_paged_prefill", "pg_plan_paged_prefill_ring", "pg_plan_destroy", "pg_plan_info", "pg_rope_table",
+EXPORTED = ["pg_plan_paged_prefill", "pg_plan_paged_prefill_ring", "pg_plan_paged_segment",
+            "pg_attn_paged_prefill_lse", "pg_attn_paged_prefill_hd512_lse", "pg_merge_attn_states",
+            "pg_plan_destroy", "pg_plan_info", "pg_rope_table",
             "pg_prep_paged_hd256", "pg_prep_paged_hd512", "pg_workspace_bytes",
             "pg_attn_paged_prefill", "pg_attn_paged_prefill_hd512", "pg_device_status",
             "pg_launch_count", "pg_status_string"]

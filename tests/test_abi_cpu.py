@@ -101,3 +101,35 @@ def test_ring_plan_rejects_before_touching_cuda():
     assert _ring_plan(8, 1, 0, -1)[0] == pg.PG_ERR_WINDOW
     assert _ring_plan(0, 1, 0, 0)[0] == pg.PG_ERR_ARG          # a request with no pages
     assert pg.pg_launch_count() == before
+
+
+def _segment_plan(kv_start, qo_len=4, start=100, pages=2, last=16):
+    return pg.pg_plan_paged_segment(
+        None, 1, np.array([0, qo_len], np.int64), np.array([0, pages], np.int64),
+        np.arange(pages, dtype=np.int32), np.array([last], np.int32),
+        np.array([kv_start], np.int64), np.array([start], np.int64), 16, 8, 256, 16, stream=0)
+
+
+def test_segment_plan_rejects_before_touching_cuda():
+    before = pg.pg_launch_count()
+    assert _segment_plan(-1)[0] == pg.PG_ERR_ARG                  # negative segment start
+    assert _segment_plan(100, qo_len=4, start=100)[0] == pg.PG_ERR_COVERAGE  # keys past the step
+    assert _segment_plan(0, last=17)[0] == pg.PG_ERR_LAST_PAGE_LEN
+    assert pg.pg_plan_paged_segment(None, 1, np.array([0, 1], np.int64), np.array([0, 1], np.int64),
+                                    np.zeros(1, np.int32), np.ones(1, np.int32), None,
+                                    np.array([5], np.int64), 16, 8, 256, 16, stream=0)[0] == pg.PG_ERR_ARG
+    assert pg.pg_launch_count() == before
+
+
+def test_merge_and_lse_entries_reject_bad_arguments():
+    before = pg.pg_launch_count()
+    assert pg.pg_merge_attn_states(0, 0, 0, 0, 0, 0, 0, 256, stream=0) == pg.PG_OK      # nothing to merge
+    assert pg.pg_merge_attn_states(0, 0, 0, 0, 0, 0, -1, 256, stream=0) == pg.PG_ERR_ARG
+    assert pg.pg_merge_attn_states(0, 0, 0, 0, 0, 0, 4, 12, stream=0) == pg.PG_ERR_ARG  # head_dim % 8
+    assert pg.pg_merge_attn_states(0, 0, 0, 0, 0, 0, 4, 256, stream=0) == pg.PG_ERR_ARG  # null inputs
+    assert pg.pg_merge_attn_states(16, 4, 16, 4, 16, 4, 1 << 31, 256, stream=0) == pg.PG_ERR_I32_OVERFLOW
+    assert pg.pg_merge_attn_states(16, 4, 24, 4, 16, 4, 4, 256, stream=0) == pg.PG_ERR_ALIGN
+    d = pg.pg_pool_t()
+    assert pg.pg_attn_paged_prefill_lse(None, d, 0, 0, 0, 0, -1, 1.0, stream=0) == pg.PG_ERR_ARG
+    assert pg.pg_attn_paged_prefill_hd512_lse(None, d, 0, 0, 0, 0, -1, 1.0, stream=0) == pg.PG_ERR_ARG
+    assert pg.pg_launch_count() == before
