@@ -214,6 +214,28 @@ def dist_setup():
     return world, rank, local
 
 
+def rank_seeds(rank: int):
+    """Seeds of this rank's prefill and decode requests: every rank owns its own requests
+    (weak scaling, no exchange step on the path)."""
+    return 1005 + 7919 * rank, 1004 + 7919 * rank
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's (equal-sized) work over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -274,8 +296,9 @@ def run_ours(args):
     peaks = load_peaks()
     stream = torch.cuda.current_stream()
     # each rank owns its own requests (weak scaling; no exchange step on this path)
-    wl5 = W.make_workload(5, seed=1005 + 7919 * rank)
-    wl4 = W.make_workload(4, seed=1004 + 7919 * rank)
+    seed5, seed4 = rank_seeds(rank)
+    wl5 = W.make_workload(5, seed=seed5)
+    wl4 = W.make_workload(4, seed=seed4)
     fams = [("prefill hd256", wl5.families[0]), ("prefill hd512", wl5.families[1]),
             ("decode hd256", wl4.families[0]), ("decode hd512", wl4.families[1])]
     runs = [(name, FamilyRun(fi, stream=stream)) for name, fi in fams]
@@ -322,15 +345,11 @@ def run_ours(args):
     # per-call durations (ms), averaged over steps
     seg = np.array([[all_evs[k][i].elapsed_time(all_evs[k][i + 1]) for i in range(n_ev - 1)]
                     for k in range(args.steps)])
-    t_step = float(seg.sum(axis=1).mean())
-    if world > 1:
-        t = torch.tensor([t_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_step = float(t.item())
+    t_step = max_over_ranks(float(seg.sum(axis=1).mean()), world, "cuda")
     avg = seg.mean(axis=0)
     flops = [attn_flops(fi) for _, fi in fams]
     total_flops = sum(flops)
-    value = world * total_flops / (t_step * 1e-3) / 1e12
+    value = job_value(world, total_flops, t_step)
 
     kernels = {}
     for i, (name, fi) in enumerate(fams):
@@ -427,12 +446,8 @@ def run_ours(args):
         e0, e1 = e2e_step()
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    t_e2e = float(np.mean(e2e_ms))
-    if world > 1:
-        t = torch.tensor([t_e2e], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_e2e = float(t.item())
-    e2e = {"value": world * total_flops / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+    t_e2e = max_over_ranks(float(np.mean(e2e_ms)), world, "cuda")
+    e2e = {"value": job_value(world, total_flops, t_e2e), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e}
 
     if rank == 0:
