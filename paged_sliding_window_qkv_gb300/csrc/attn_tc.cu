@@ -557,6 +557,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t bytes = (uint32_t)__popc((bm_load >> sh) & box_mask) * box_bytes;
         const bool issue = my_t == tb && ((bm_load >> lane) & 1u);
         const int nparts = is_v ? 1 : KP;
+        if (!is_v && KP > 1 && !fix) {
+          // every K part of the tile in one copy instruction (each warp-level copy instruction
+          // costs the producer hundreds of cycles, whatever its box count): lane i copies box
+          // i mod nbox of part i / nbox, after lane 0 has seen every part's slot free and
+          // announced each part's bytes
+          int r = 1;
+          if (lane == 0) {
+            for (int pp = 0; r && pp < KP; ++pp)
+              r = mbar_wait_inline(EMPTY(KSLOT(JJ, pp)), (KROUND(JJ, pp) & 1) ^ 1, abort_flag,
+                                   a.status) ? 1 : 0;
+            if (r)
+              for (int pp = 0; pp < KP; ++pp) mbar_expect_tx_cl_relaxed(LEAD(FULL(KSLOT(JJ, pp))), bytes);
+          }
+          if (!__shfl_sync(0xffffffffu, r, 0)) {
+            ok = false;
+            break;
+          }
+          const int pp = lane / nbox, b = lane % nbox;
+          const int32_t row = __shfl_sync(0xffffffffu, my_row, sh + b);
+          const bool go = pp < KP && ((bm_load >> (sh + b)) & 1u);
+          if (go) {
+            const int s = KSLOT(JJ, pp);
+            tma_load_4d(sSlots + s * kSlotBytes + b * (BR * 512), &tm_kv, 0, 0, pp * 4, row / 8,
+                        LEAD(FULL(s)));
+          }
+          continue;
+        }
         for (int pp = 0; ok && pp < nparts; ++pp) {
           const int s = is_v ? VSLOT(JJ) : KSLOT(JJ, pp);
           const int round = is_v ? (int)(JJ / NVR) : KROUND(JJ, pp);
