@@ -88,21 +88,36 @@ def decode_bytes(fi):
 
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock and throttle samples every 100 ms; only the samples taken inside the
+    timed window (mark_start / mark_stop, host time) are summarised. The raw CSV goes to
+    $PG_CLOCK_LOG (a directory) when set, else to a temporary file."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index):
+        import tempfile
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        log_dir = os.environ.get("PG_CLOCK_LOG")
+        if log_dir:
+            self.path = os.path.join(log_dir, f"clocks_rank{device_index}.csv")
+        else:
+            self.path = os.path.join(tempfile.gettempdir(), f"pg_clocks_{os.getpid()}_{device_index}.csv")
         self.dev = device_index
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
 
     def start(self):
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                   "-lms", "200"]
+                   "-lms", "100"]
             uuid = None
             try:
                 import torch
@@ -125,21 +140,29 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
+        import datetime
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-        if not rows:
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None
+                  and self.t0 <= r[0] <= self.t1]
+        window = "timed region"
+        if not inside:  # a window shorter than the sampling period: the nearest samples
+            inside, window = rows, "around the timed region"
+        if not inside:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl) if v == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({names[i] for _, _, _, fl in inside for i, v in enumerate(fl)
+                          if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": inside[0][2],
+                "reasons": reasons, "samples": len(inside), "window": window}
 
 
 # ---------------------------------------------------------------------------- oracle leg
@@ -317,6 +340,10 @@ def run_ours(args):
         if evs is not None:
             evs[i].record(stream)
 
+    # the clock sampler runs from before the warm-up, so it is sampling when the timed region
+    # starts; only samples inside the timed region are summarised
+    sampler = ClockSampler(local)
+    sampler.start()
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -324,18 +351,18 @@ def run_ours(args):
     n_ev = 2 * len(runs) + 1
     all_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
                for _ in range(args.steps)]
-    sampler = ClockSampler(local)
-    sampler.start()
     launches0 = pg.pg_launch_count()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    sampler.mark_start()
     for k in range(args.steps):
         # the flush is queued ahead of the step (no host sync in between), so the step's first
         # event does not also time the host's launch of its first call
         flush.zero_()
         step(all_evs[k])
     torch.cuda.synchronize()
+    sampler.mark_stop()
     if world > 1:
         torch.distributed.barrier()
     launches = pg.pg_launch_count() - launches0
@@ -476,7 +503,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
