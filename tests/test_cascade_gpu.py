@@ -179,3 +179,22 @@ def test_prep_on_a_suffix_segment_writes_its_slots_and_the_prefix_plan_refuses_p
     PT.prep_gate(device_to_bits(q_out), qo, "q_out")
     suf.close()
     pre.close()
+
+
+def test_segment_decode_without_allocation_matches_the_workspace_path():
+    hq, hkv = FAMS[512]
+    D = 512
+    rng = np.random.Generator(np.random.PCG64(5150))
+    ci = W.make_cascade(rng, 1100, [700, 20, 3], [1, 1, 1], 16, hq, hkv, D)
+    pool = bits_to_device(fill_pool(ci, full=False))
+    desc = pg.pool_descriptor(pool)
+    q = bits_to_device(ci.q)
+    R = ci.full.num_req
+    for b, ks in ((ci.prefix, np.zeros(R, np.int64)), (ci.suffix, np.full(R, 1100, np.int64))):
+        plan = plan_of(b, hq, hkv, D, ks)
+        ref, _ = attn_lse(plan, desc, q, D, -1, 0.06)
+        out = torch.empty_like(ref)
+        pg.check(pg.pg_attn_paged_decode_noalloc(plan, desc, 0, q, out, -1, 0.06), "noalloc decode")
+        torch.cuda.synchronize()
+        assert np.array_equal(device_to_bits(out), device_to_bits(ref))
+        plan.close()

@@ -10,8 +10,10 @@ brute force over the true history.
 """
 import numpy as np
 import pytest
+import torch
 
 import parity as PT
+from oracle import oracle as O
 from paged_sliding_window_qkv_gb300 import pg
 from paged_sliding_window_qkv_gb300 import workloads as W
 from paged_sliding_window_qkv_gb300.runner import FamilyRun, device_to_bits
@@ -79,3 +81,30 @@ def test_ring_plan_bounds_the_attention_window():
     assert run.attn_status(window_left=-1) == pg.PG_ERR_WINDOW
     assert pg.pg_launch_count() == before
     run.close()
+
+
+def test_ring_plan_lse_matches_oracle():
+    # one prefill step past the window through a wrapped ring, with the log-sum-exp output
+    D, hq, hkv = 256, 16, 8
+    rng = np.random.Generator(np.random.PCG64(91))
+    R = -(-(WIN + 40) // PS)
+    num_pages = R + 3
+    pages = rng.permutation(num_pages)[:R].astype(np.int32)
+    pool_bits = W.bf16_normal(rng, (1, num_pages, 2, hkv, PS, D))
+    qo, start = np.array([0, 40], np.int64), np.array([700], np.int64)
+    indptr = np.array([0, R], np.int64)
+    rc, plan = pg.pg_plan_paged_prefill_ring(None, 1, qo, indptr, pages, start, hq, hkv, D, PS, WIN)
+    pg.check(rc, "ring plan")
+    pool = torch.from_numpy(pool_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    q_bits = W.bf16_normal(rng, (40, hq, D))
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty(40, hq, dtype=torch.float32, device="cuda")
+    pg.check(pg.pg_attn_paged_prefill_lse(plan, pg.pool_descriptor(pool), 0, q, out, lse, WIN, 0.06),
+             "attention+lse")
+    torch.cuda.synchronize()
+    ref_o, ref_l = O.attention(q_bits, pool_bits, 0, qo, indptr, pages, None, start, hkv, WIN, 0.06,
+                               ring=True, return_lse=True)
+    PT.attn_gate(O.bf16_to_f64(device_to_bits(out)), ref_o, "ring + lse")
+    assert np.abs(lse.cpu().numpy() - ref_l).max() <= 1e-2
+    plan.close()
