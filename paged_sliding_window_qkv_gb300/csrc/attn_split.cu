@@ -4,10 +4,11 @@
 //
 // One CTA owns BM query rows that share one KV head (GQA: rows are (token, head)
 // pairs of the head group, so each K/V tile is loaded once for the whole group) and
-// walks the KV tiles of its visible key range. K/V rows are gathered page by page
-// with cp.async into XOR-swizzled shared memory, double-buffered. S = Q K^T and
-// O += P V run on bf16 mma.sync with fp32 accumulation; the online softmax runs in
-// fp32 in log2 units.
+// walks the KV tiles of its visible key range. K/V rows are gathered row by row (one page
+// lookup per key row; ring plans wrap the page index, key-segment plans offset it by the
+// segment's first position) with cp.async into XOR-swizzled shared memory through NS
+// stages. S = Q K^T and O += P V run on bf16 mma.sync with fp32 accumulation; the online
+// softmax runs in fp32 in log2 units, and the row's log-sum-exp is written when asked.
 //
 // Two grid forms share the kernel:
 //   prefill: one CTA per (work item = request x query tile, KV head);

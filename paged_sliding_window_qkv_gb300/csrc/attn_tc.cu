@@ -4,30 +4,33 @@
 // division; "feat(gemma4): paged KV serving across both attention families",
 // Description: hd256 local layers with a sliding window, hd512 global layers causal).
 //
-// Work unit: a 128-row query tile that packs the GQA group of one KV head (rows are
-// token-major, head-minor, exactly the order a 3-D TMA box of q[token][head][d] lands in
-// shared memory) and one 256-column part of the output; the unit walks the 64-key tiles of its
-// visible key range, skipping tiles outside the causal window. The kernel is persistent: one
-// CTA per SM (its shared and tensor memory fill the SM) takes one unit of each round of
-// gridDim.x units (longest first), so the barriers, tensor memory and K/V rings
-// carry over from unit to unit: the producers fetch the next unit's first tiles while the
-// current one finishes, and the next unit's Q enters TMEM before this unit's epilogue.
+// Work unit: a pair of adjacent 128-row query tiles (rows pack the GQA group of one KV head,
+// token-major, head-minor) and one 256-column part of the output, run by the two CTAs of a
+// cluster; the unit walks the 64-key tiles of the pair's visible key range, skipping tiles
+// outside the causal window. The kernel is persistent: one CTA per SM (its shared and tensor
+// memory fill the SM), each cluster taking one unit per round (longest first), so barriers,
+// tensor memory and K/V rings carry over from unit to unit: the producers fetch the next
+// unit's first tiles while the current one finishes, and the next unit's Q enters TMEM before
+// this unit's epilogue.
 //
-//   warp 0     K producer (TMA): one 4-D box per page (BR rows x 256 d) into a ring of
-//              three 32 KB part slots; also each unit's Q columns [256,512) (head_dim 512)
-//   warp 10    V producer (TMA): one 3-D box per page into NVR 32 KB slots
-//   warp 1     QK issuer: S = Q K^T into a TMEM S buffer (M=128, N=64, K=16 steps; the
-//              first 256-d part reads Q from TMEM, head_dim 512's second part from shared
-//              memory)
-//   warp 11    PV issuer: O += P V into TMEM (M=128, N=256, K=16 steps; P from shared
-//              memory for head_dim 256, from TMEM over S for head_dim 512); MMAs are issued
-//              by lane 0, completion signalled with tcgen05.commit
-//   warps 2..9 softmax: first Q columns [0,256) into TMEM; then two threads per query row
-//              (each reads the whole S row for the maximum, exponentiates half of the tile's
-//              keys and owns half of O's columns), masked on boundary tiles only, online
-//              softmax in log2 units with lazy rescaling (O is rescaled in TMEM only when a
-//              row maximum outgrows a 2^64 headroom by more than 2^48: bf16 P and fp32 O and
-//              row sums hold the range, and O / l is unchanged); then the epilogue
+//   warp 0     K producer (TMA): this CTA's 32 keys of each tile, one 4-D box per page
+//              (BR rows x 256 d) into 16 KB part slots; box coordinates and page ids are
+//              worked out a batch of tiles ahead, and a head_dim 512 tile's two parts go out
+//              in one copy instruction; also each unit's Q columns [256,512) (head_dim 512)
+//   warp 10    V producer (TMA): this CTA's 128 output columns of each tile, one 3-D box per
+//              page into 16 KB slots
+//   warp 1     QK issuer (leader CTA): S = Q K^T into a TMEM S buffer (2-SM MMA, M=256, N=64,
+//              K=16 steps; the first 256-d part reads Q from TMEM, head_dim 512's second part
+//              from shared memory)
+//   warp 11    PV issuer (leader CTA): O += P V into TMEM (M=256, N=256, K=16 steps; P from
+//              shared memory); MMAs are issued by lane 0, completion signalled with
+//              tcgen05.commit multicast to both CTAs
+//   warps 2..9 softmax: the unit's first Q columns [0,256) into TMEM; then two threads per
+//              query row (each reads the whole S row for the maximum, exponentiates half of
+//              the tile's keys and owns half of O's columns), masked on boundary tiles only,
+//              online softmax in log2 units with lazy rescaling (O is rescaled in TMEM only
+//              when a row maximum outgrows a 2^64 headroom by more than 2^48: bf16 P and fp32
+//              O and row sums hold the range, and O / l is unchanged); then the epilogue
 //              normalises O and each thread stores its 256 contiguous bytes of the row.
 //
 // O holds 256 output columns: for head_dim 512 each query tile is two units, each computing
@@ -71,8 +74,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 //
 // TMEM map (each CTA, 512 columns): O [0,256) (the unit's 256 output columns), Q columns
 // [256,384) (this unit's first 256-d part of Q; QK reads A from TMEM), two S buffers
-// [384,448) and [448,512). The softmax writes P(j) to one of two 16 KB shared-memory buffers
-// (PV is SS), so QK(j + 2) waits only for both CTAs' reads of S(j). head_dim 512 also keeps Q
+// [384,448) and [448,512). The softmax writes P(j) to a 16 KB shared-memory buffer (NPB of
+// them; PV is SS), so QK(j + 2) waits only for both CTAs' reads of S(j). head_dim 512 also keeps Q
 // columns [256,512) in shared memory (64 KB; QK's second part is SS). K streams through NKS
 // 256-d part slots (a tile is KP parts), V through NVR tile slots.
 template <int DQK>
@@ -90,7 +93,7 @@ struct TcCfg {
   static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
   static constexpr int NBAR = 2 * NS + 22;      // ..., QFREE, 4 per-producer fix-up barriers last
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
-  static constexpr int NSB = 2;                 // S buffers (and P buffers)
+  static constexpr int NSB = 2;                 // S buffers (and PFULL / PVDONE barrier pairs)
   static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };

@@ -12,7 +12,8 @@
 // row is one conflict-free 512-byte read per warp), the RMS reduction is a warp shuffle, each
 // lane holds both elements of its rotary pairs, and every
 // result row is one coalesced 512-byte (or 1 KB) store: q_out rows, or K/V rows at the
-// token's paged slot. The producer also resolves each token's request, position and page
+// token's paged slot (slot = position, wrapped over the request's pages for a ring plan, or
+// counted from the segment's first position for a key-segment plan). The producer also resolves each token's request, position and page
 // (32 tokens at a time, one per lane) and passes them to the consumers in the stage header.
 //
 // Waits are bounded (two seconds of %globaltimer); a wait that runs out sets the device
