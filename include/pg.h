@@ -128,9 +128,11 @@ int pg_plan_paged_prefill(pg_plan_t* plan, int32_t num_req, const int64_t* qo_in
  *
  * Inputs as for pg_plan_paged_prefill, without last_page_len (the ring has no last page):
  *   window_left  >= 0: the largest window attention may run with on this plan.
- * Coverage: pages_r * page_size >= window_left + qo_len_r for every request, so no key
- * that a query of the step can see is overwritten by the step's own writes
- * (PG_ERR_COVERAGE otherwise); window_left < 0 fails with PG_ERR_WINDOW. A request may
+ * Coverage: pages_r * page_size >= window_left + qo_len_r, or no position has wrapped yet
+ * (start_pos_r + qo_len_r <= pages_r * page_size), for every request, so no key that a
+ * query of the step can see is overwritten by the step's own writes (PG_ERR_COVERAGE
+ * otherwise); window_left < 0 fails with PG_ERR_WINDOW. A ring may so grow page by page
+ * while the request is shorter than it. A request may
  * start at any position (start_pos is not bounded by its pages), and all positions
  * below start_pos_r must have been written through the same ring by earlier steps.
  * Attention on a ring plan requires 0 <= window_left <= the plan's window

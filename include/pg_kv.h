@@ -51,6 +51,18 @@ enum { PG_KV_LOCAL = 0, PG_KV_GLOBAL = 1 };  /* the two families: hd256 local, h
 int pg_kv_server_create(pg_kv_server_t* out, int32_t pages_local, int32_t pages_global,
                         int32_t page_size, int32_t window_left, int32_t fail_closed_at_window,
                         int32_t rope_rows);
+/* A server whose local family keeps a ring of pages instead of failing closed at the window
+ * ("gemma4: serving prep needs pool-write forms", Proposed Plan: callers that cross the
+ * window need a separate slot mapping; the mapping is pg_plan_paged_prefill_ring's). Each
+ * request's local family holds at most ring = ceil((window_left + ring_max_step) / page_size)
+ * pages: ceil(frontier / page_size) while that is smaller, then the same ring pages, reused.
+ * Steps are at most ring_max_step (>= 1) tokens (PG_KV_ERR_WINDOW otherwise, nothing
+ * changed); the global family grows with the frontier as in pg_kv_server_create. The local
+ * family's batch plan inputs feed pg_plan_paged_prefill_ring with window_left (its
+ * last_page_len output is not read there). Other arguments and errors as pg_kv_server_create. */
+int pg_kv_server_create_ring(pg_kv_server_t* out, int32_t pages_local, int32_t pages_global,
+                             int32_t page_size, int32_t window_left, int32_t ring_max_step,
+                             int32_t rope_rows);
 void pg_kv_server_destroy(pg_kv_server_t srv);
 
 /* Open a request (frontier 0, no pages) and return its id (> 0, never reused by this server). */
@@ -61,7 +73,8 @@ int pg_kv_request_close(pg_kv_server_t srv, int64_t request_id);
 
 /* Admit one step of `n_tokens` (>= 1) new positions for a request, in both families at once.
  * The page count per family is the exact frontier account: ceil((frontier + n_tokens) /
- * page_size) minus the pages the family already holds. Before anything changes, the request
+ * page_size) (capped at the ring for the local family of a ring server) minus the pages the
+ * family already holds. Before anything changes, the request
  * must belong to this server, both families must sit at the same frontier and hold exactly the
  * pages it accounts for, and the window and rotary bounds must hold. Then both families'
  * pages are reserved; if either pool refuses, the other reservation is dropped and
@@ -86,7 +99,9 @@ int pg_kv_free_pages(pg_kv_server_t srv, int32_t family, int32_t* n);
 int pg_kv_inject_refusal(pg_kv_server_t srv, int32_t family, int32_t count);
 
 /* Plan inputs of a batch for one family, after each request's admitted step of step_tokens[i]
- * tokens: kv_page_indptr [n + 1], page_ids (cap entries), last_page_len [n], start_pos [n]
+ * tokens: kv_page_indptr [n + 1], page_ids (cap entries, in position order, or ring order for a
+ * ring server's local family), last_page_len [n] (the frontier's slot count in its page),
+ * start_pos [n]
  * (= frontier - step_tokens[i]), in the layout pg_plan_paged_prefill reads. Each step must be
  * no longer than the request's frontier. *n_page_ids receives the page-id count. */
 int pg_kv_batch_plan_inputs(pg_kv_server_t srv, int32_t family, int32_t n,

@@ -150,7 +150,9 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
       int64_t cap = 0, need = 0;
       if (!mul_i64(k1 - k0, ps, &cap) || !add_i64(ring_window, qo_len, &need))
         return PG_ERR_I32_OVERFLOW;
-      if (cap < need) return PG_ERR_COVERAGE;  // the ring cannot hold the window plus the step
+      // a step's write can cover a key one of its queries sees only if some position wraps
+      // (pos_end > cap) and the ring is shorter than the window plus the step
+      if (cap < need && pos_end > cap) return PG_ERR_COVERAGE;
       kv_len = pos_end;
       // the position's slot in its (ring) page; last_page_len is not used in ring addressing
       lpl = (int32_t)(pos_end - ((pos_end - 1) / ps) * ps);

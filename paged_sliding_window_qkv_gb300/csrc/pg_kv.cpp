@@ -24,6 +24,9 @@ int32_t pages_for(int64_t len, int32_t ps) { return (int32_t)((len + ps - 1) / p
 
 struct pg_kv_server {
   int32_t page_size = 0, window_left = 0, fail_closed = 0, rope_rows = 0;
+  // ring mode (0: off): the local family holds at most ring_pages pages per request, reused as
+  // a ring once the frontier passes them; steps are at most ring_max_step tokens
+  int32_t ring_pages = 0, ring_max_step = 0;
   std::set<int32_t> free_pages[2];  // lowest id first
   int32_t refusals[2] = {0, 0};     // injected refusals still to come
   int64_t next_id = 1;
@@ -47,11 +50,17 @@ struct pg_kv_server {
   void give_back(int family, const std::vector<int32_t>& pages) {
     free_pages[family].insert(pages.begin(), pages.end());
   }
+  // Pages a family holds at a frontier: ceil(frontier / page_size), capped at the ring for
+  // the local family in ring mode.
+  int32_t held_for(int family, int64_t frontier) const {
+    const int32_t n = pages_for(frontier, page_size);
+    return (family == PG_KV_LOCAL && ring_pages > 0 && n > ring_pages) ? ring_pages : n;
+  }
   // The frontier account: both families at one frontier, each holding exactly its pages.
   bool consistent(const KvRequest& r) const {
     if (r.frontier[0] != r.frontier[1]) return false;
     for (int f = 0; f < 2; ++f)
-      if ((int64_t)r.pages[f].size() != pages_for(r.frontier[f], page_size)) return false;
+      if ((int64_t)r.pages[f].size() != held_for(f, r.frontier[f])) return false;
     return true;
   }
 };
@@ -73,6 +82,20 @@ int pg_kv_server_create(pg_kv_server_t* out, int32_t pages_local, int32_t pages_
   for (int32_t p = 0; p < pages_local; ++p) s->free_pages[PG_KV_LOCAL].insert(p);
   for (int32_t p = 0; p < pages_global; ++p) s->free_pages[PG_KV_GLOBAL].insert(p);
   *out = s;
+  return PG_KV_OK;
+}
+
+int pg_kv_server_create_ring(pg_kv_server_t* out, int32_t pages_local, int32_t pages_global,
+                             int32_t page_size, int32_t window_left, int32_t ring_max_step,
+                             int32_t rope_rows) {
+  if (ring_max_step < 1 || page_size <= 0 || window_left < 0) return PG_KV_ERR_ARG;
+  const int64_t ring = ((int64_t)window_left + ring_max_step + page_size - 1) / page_size;
+  if (ring > INT32_MAX) return PG_KV_ERR_ARG;
+  const int rc = pg_kv_server_create(out, pages_local, pages_global, page_size, window_left, 0,
+                                     rope_rows);
+  if (rc != PG_KV_OK) return rc;
+  (*out)->ring_pages = (int32_t)ring;
+  (*out)->ring_max_step = ring_max_step;
   return PG_KV_OK;
 }
 
@@ -105,10 +128,11 @@ int pg_kv_admit_step(pg_kv_server_t srv, int64_t request_id, int32_t n_tokens) {
   const int64_t len = (int64_t)r.frontier[0] + n_tokens;
   if (len > INT32_MAX) return PG_KV_ERR_ARG;
   if (srv->fail_closed && len > (int64_t)srv->window_left + 1) return PG_KV_ERR_WINDOW;
+  // a ring holds the window plus at most ring_max_step new positions
+  if (srv->ring_pages > 0 && n_tokens > srv->ring_max_step) return PG_KV_ERR_WINDOW;
   if (len > srv->rope_rows) return PG_KV_ERR_ROPE;
   int32_t need[2];
-  for (int f = 0; f < 2; ++f)
-    need[f] = pages_for(len, srv->page_size) - (int32_t)r.pages[f].size();
+  for (int f = 0; f < 2; ++f) need[f] = srv->held_for(f, len) - (int32_t)r.pages[f].size();
   // reserve both before committing either; a refused side drops the other
   std::vector<int32_t> got[2];
   if (!srv->reserve(PG_KV_LOCAL, need[PG_KV_LOCAL], &got[PG_KV_LOCAL])) return PG_KV_ERR_NO_PAGES;
@@ -189,7 +213,8 @@ int pg_kv_batch_plan_inputs(pg_kv_server_t srv, int32_t family, int32_t n,
     for (size_t k = 0; k < p.size(); ++k) page_ids[off + (int64_t)k] = p[k];
     off += (int64_t)p.size();
     kv_page_indptr[i + 1] = off;
-    last_page_len[i] = r.frontier[family] - ((int32_t)p.size() - 1) * srv->page_size;
+    // the frontier's slot count in its page (a ring plan does not read it)
+    last_page_len[i] = r.frontier[family] - ((r.frontier[family] - 1) / srv->page_size) * srv->page_size;
     start_pos[i] = (int64_t)r.frontier[family] - step_tokens[i];
   }
   *n_page_ids = (int32_t)total;

@@ -362,6 +362,21 @@ def pg_kv_server_create(pages_local, pages_global, page_size, window_left, fail_
     return rc, (h if rc == PG_KV_OK else None)
 
 
+_lib.pg_kv_server_create_ring.argtypes = [C.POINTER(C.c_void_p), C.c_int32, C.c_int32, C.c_int32,
+                                          C.c_int32, C.c_int32, C.c_int32]
+_lib.pg_kv_server_create_ring.restype = C.c_int
+
+
+def pg_kv_server_create_ring(pages_local, pages_global, page_size, window_left, ring_max_step,
+                             rope_rows):
+    """Server whose local family keeps a ring of pages. Returns (status, handle or None)."""
+    h = C.c_void_p()
+    rc = _lib.pg_kv_server_create_ring(C.byref(h), int(pages_local), int(pages_global),
+                                       int(page_size), int(window_left), int(ring_max_step),
+                                       int(rope_rows))
+    return rc, (h if rc == PG_KV_OK else None)
+
+
 def pg_kv_server_destroy(srv) -> None:
     _lib.pg_kv_server_destroy(srv)
 
@@ -427,6 +442,6 @@ def pg_kv_batch_plan_inputs(srv, family, request_ids, step_tokens, cap=1 << 20):
     return rc, indptr, pages[:cnt.value].copy(), last[:n].copy(), start[:n].copy()
 
 
-EXPORTED += ["pg_kv_server_create", "pg_kv_server_destroy", "pg_kv_request_open",
+EXPORTED += ["pg_kv_server_create", "pg_kv_server_create_ring", "pg_kv_server_destroy", "pg_kv_request_open",
              "pg_kv_request_close", "pg_kv_admit_step", "pg_kv_request_info", "pg_kv_request_pages",
              "pg_kv_free_pages", "pg_kv_inject_refusal", "pg_kv_batch_plan_inputs"]

@@ -133,3 +133,11 @@ def test_merge_and_lse_entries_reject_bad_arguments():
     assert pg.pg_attn_paged_prefill_lse(None, d, 0, 0, 0, 0, -1, 1.0, stream=0) == pg.PG_ERR_ARG
     assert pg.pg_attn_paged_prefill_hd512_lse(None, d, 0, 0, 0, 0, -1, 1.0, stream=0) == pg.PG_ERR_ARG
     assert pg.pg_launch_count() == before
+
+
+def test_ring_plan_accepts_a_ring_that_has_not_wrapped_yet():
+    # 2 pages x 16 = 32 slots < window 100 + 20 tokens, but positions 0..19 never wrap: the
+    # coverage check passes (the build then needs a GPU for its upload)
+    rc = _ring_plan(2, 20, 0, 100)[0]
+    assert rc != pg.PG_ERR_COVERAGE
+    assert _ring_plan(2, 20, 13, 100)[0] == pg.PG_ERR_COVERAGE   # positions 13..32 wrap

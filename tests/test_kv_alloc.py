@@ -179,3 +179,39 @@ def test_random_traffic_keeps_the_books():
             f, nl, ng, _, _ = state(s, r)
             assert nl == ng == -(-f // 8)
     pg.pg_kv_server_destroy(s)
+
+
+def test_ring_server_caps_the_local_family_at_its_ring():
+    ps, window, max_step = 16, 100, 64
+    ring = -(-(window + max_step) // ps)                 # 11 pages
+    rc, s = pg.pg_kv_server_create_ring(40, 64, ps, window, max_step, 1 << 20)
+    assert rc == pg.PG_KV_OK
+    rid = open_req(s)
+    frontier = 0
+    for n in [37, 20, 64, 1, 50, 64, 1, 64, 3, 64, 64]:
+        assert pg.pg_kv_admit_step(s, rid, n) == pg.PG_KV_OK
+        frontier += n
+        f, nl, ng, local, _ = state(s, rid)
+        assert f == frontier
+        assert nl == min(-(-frontier // ps), ring)      # grows, then stays at the ring
+        assert ng == -(-frontier // ps)                  # the global family keeps growing
+        assert free(s) == (40 - nl, 64 - ng)
+    assert frontier > 2 * ring * ps                      # wrapped more than once
+    # a step longer than the ring allows beside the window is refused, nothing changed
+    before = free(s), state(s, rid)
+    assert pg.pg_kv_admit_step(s, rid, max_step + 1) == pg.PG_KV_ERR_WINDOW
+    assert (free(s), state(s, rid)) == before
+    # plan inputs: the ring's pages in ring order, start = frontier - step
+    rc, indptr, pages, last, start = pg.pg_kv_batch_plan_inputs(s, L, [rid], [3])
+    assert rc == pg.PG_KV_OK
+    assert tuple(pages) == state(s, rid)[3] and len(pages) == ring
+    assert start[0] == frontier - 3 and last[0] == (frontier - 1) % ps + 1
+    assert pg.pg_kv_request_close(s, rid) == pg.PG_KV_OK
+    assert free(s) == (40, 64)
+    pg.pg_kv_server_destroy(s)
+
+
+def test_ring_server_rejects_bad_arguments():
+    assert pg.pg_kv_server_create_ring(8, 8, 16, 100, 0, 1 << 20)[0] == pg.PG_KV_ERR_ARG
+    assert pg.pg_kv_server_create_ring(8, 8, 0, 100, 8, 1 << 20)[0] == pg.PG_KV_ERR_ARG
+    assert pg.pg_kv_server_create_ring(8, 8, 16, -1, 8, 1 << 20)[0] == pg.PG_KV_ERR_ARG

@@ -55,3 +55,40 @@ def test_allocator_pages_drive_prep_and_attention():
         assert pg.pg_kv_request_close(srv, r) == pg.PG_KV_OK
     assert pg.pg_kv_free_pages(srv, pg.PG_KV_LOCAL)[1] == num_pages
     pg.pg_kv_server_destroy(srv)
+
+
+def test_ring_server_pages_carry_the_local_family_past_its_window():
+    # the local family on a ring server (window 100, steps of up to 64 tokens: 11-page rings)
+    # and the global family growing linearly, stepped until every ring has wrapped
+    win, max_step = 100, 64
+    pages = {pg.PG_KV_LOCAL: 36, pg.PG_KV_GLOBAL: 64}
+    rc, srv = pg.pg_kv_server_create_ring(pages[pg.PG_KV_LOCAL], pages[pg.PG_KV_GLOBAL], PS, win,
+                                          max_step, 4096)
+    assert rc == pg.PG_KV_OK
+    rids = [pg.pg_kv_request_open(srv)[1] for _ in range(3)]
+    rng = np.random.Generator(np.random.PCG64(4242))
+    pools = {}
+    schedule = [[37, 20, 16], [1, 1, 1], [64, 50, 64], [1, 1, 1], [64, 64, 30], [1, 1, 1],
+                [64, 1, 64], [1, 1, 1], [64, 64, 64], [64, 64, 64], [1, 1, 1]]
+    for steps in schedule:
+        for r, n in zip(rids, steps):
+            assert pg.pg_kv_admit_step(srv, r, n) == pg.PG_KV_OK
+        for fam_id in (pg.PG_KV_LOCAL, pg.PG_KV_GLOBAL):
+            ring = fam_id == pg.PG_KV_LOCAL
+            fi = step_inputs(srv, fam_id, rids, steps, pages[fam_id], rng, 7)
+            before = pools.get(fam_id)
+            run = FamilyRun(fi, pool_bits=before, rope_rows=4096, ring_window=win if ring else None)
+            run.prep()
+            run.attn(window_left=win if ring else None)
+            pools[fam_id] = device_to_bits(run.pool)
+            assert pg.pg_device_status() == pg.PG_OK
+            PT.check_prep(run, fi, initial_pool_bits=before, ring=ring)
+            ref = PT.attn_reference(fi, device_to_bits(run.q_out), pools[fam_id],
+                                    window_left=win if ring else None, ring=ring)
+            PT.attn_gate(PT.bf16_out(run), ref, f"family {fam_id} steps {steps}")
+            run.close()
+    f = pg.pg_kv_request_info(srv, rids[0])[1]
+    assert f > 2 * 11 * PS                                  # the first request's ring wrapped twice
+    for r in rids:
+        assert pg.pg_kv_request_close(srv, r) == pg.PG_KV_OK
+    pg.pg_kv_server_destroy(srv)
