@@ -12,7 +12,9 @@
  * This is host code only (no CUDA calls, no device memory). A server owns two page
  * allocators, one per family; each request holds a state in both: its page list and its
  * frontier (the number of KV positions written, the same in both families). The page lists
- * feed pg_plan_paged_prefill's kv_page_indptr / page_ids / last_page_len / start_pos.
+ * feed pg_plan_paged_prefill's kv_page_indptr / page_ids / last_page_len / start_pos; a ring
+ * server (pg_kv_server_create_ring) keeps the local family on a ring of pages past the window
+ * instead of failing closed, for pg_plan_paged_prefill_ring.
  *
  * Errors: int status, PG_KV_OK = 0, negative = error. On any error no state changes: both
  * pools keep their occupancy and every request keeps its pages and frontier.
