@@ -141,3 +141,17 @@ def test_ring_plan_accepts_a_ring_that_has_not_wrapped_yet():
     rc = _ring_plan(2, 20, 0, 100)[0]
     assert rc != pg.PG_ERR_COVERAGE
     assert _ring_plan(2, 20, 13, 100)[0] == pg.PG_ERR_COVERAGE   # positions 13..32 wrap
+
+
+def test_headers_are_plain_c():
+    # the boundary is a C ABI: each header compiles as strict C99 on its own
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    for h in sorted(glob.glob(os.path.join(INCLUDE, "*.h"))):
+        r = subprocess.run([cc, "-x", "c", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                            "-fsyntax-only", "-"], input=f'#include "{h}"\n', text=True,
+                           capture_output=True)
+        assert r.returncode == 0, (h, r.stderr)
