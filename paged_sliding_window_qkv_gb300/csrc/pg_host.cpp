@@ -725,7 +725,7 @@ const char* pg_status_string(int s) {
     case PG_ERR_HEADS: return "num_qo_heads is not a positive multiple of num_kv_heads";
     case PG_ERR_NONFINITE: return "non-finite or non-positive scale, eps or theta";
     case PG_ERR_ROPE_RANGE: return "a position is past the rotary tables";
-    case PG_ERR_COVERAGE: return "pages do not cover [0, start_pos + qo_len)";
+    case PG_ERR_COVERAGE: return "pages do not cover the keys the step needs (linear: exactly [0, start_pos + qo_len))";
     case PG_ERR_LAYER: return "layer outside the pool";
     case PG_ERR_LAYOUT: return "pool layout, strides or capacity inconsistent";
     case PG_ERR_PLAN_MISMATCH: return "plan geometry or tiling disagrees with the pool or kernel";
