@@ -145,10 +145,16 @@ def test_batch_plan_inputs_follow_the_plan_contract():
     pg.pg_kv_server_destroy(s)
 
 
-def test_random_traffic_keeps_the_books():
+@pytest.mark.parametrize("ring", [False, True], ids=["linear", "ring"])
+def test_random_traffic_keeps_the_books(ring):
     rng = np.random.default_rng(11)
     total = (48, 24)
-    s = server(pages_local=total[0], pages_global=total[1], ps=8, window=1 << 20)
+    ring_pages = -(-(30 + 19) // 8)  # window 30, steps of at most 19 tokens
+    if ring:
+        rc, s = pg.pg_kv_server_create_ring(total[0], total[1], 8, 30, 19, 1 << 20)
+        assert rc == pg.PG_KV_OK
+    else:
+        s = server(pages_local=total[0], pages_global=total[1], ps=8, window=1 << 20)
     live = {}
     for _ in range(600):
         op = rng.integers(4)
@@ -177,7 +183,8 @@ def test_random_traffic_keeps_the_books():
             assert all(0 <= p < total[fam] for p in held)
         for r in live:
             f, nl, ng, _, _ = state(s, r)
-            assert nl == ng == -(-f // 8)
+            assert ng == -(-f // 8)
+            assert nl == (min(ng, ring_pages) if ring else ng)
     pg.pg_kv_server_destroy(s)
 
 
