@@ -99,6 +99,7 @@ class ClockSampler:
         import tempfile
         self.proc = None
         log_dir = os.environ.get("PG_CLOCK_LOG")
+        self.keep = bool(log_dir)
         if log_dir:
             self.path = os.path.join(log_dir, f"clocks_rank{device_index}.csv")
         else:
@@ -142,7 +143,14 @@ class ClockSampler:
         self.f.close()
         import datetime
         rows = []
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
                 continue
