@@ -51,6 +51,18 @@ def test_windows_and_ragged_tiles(fam, window_left):
     parity.attn_gate(gpu, ref, f"{fam.name} W={window_left}")
 
 
+@pytest.mark.parametrize("fam", [W.HD256, W.HD512], ids=["hd256", "hd512"])
+@pytest.mark.parametrize("ps", [8, 32, 64])
+def test_tensor_core_path_at_other_page_sizes(fam, ps):
+    # the tcgen05 path copies one box of min(ps, 32) K rows / min(ps, 64) V rows per page, so
+    # page sizes 8, 32 and 64 give 4, 1 and 1 K boxes per lane batch (16 gives 2)
+    fi = W.custom_family(fam, [1, 9, 64, 130, 257], [0, 40, 3, 200, 17], seed=41 + ps,
+                         page_size=ps, spare_pages=3, pool_fill="normal",
+                         window_left=100 if fam is W.HD256 else -1)
+    gpu, ref = _attn_only(fi)
+    parity.attn_gate(gpu, ref, f"{fam.name} page size {ps}")
+
+
 def test_window_zero_returns_own_value_on_gpu():
     fi = W.custom_family(W.HD256, [37], [5], seed=37, pool_fill="normal", window_left=0)
     pool = fi.make_pool()
