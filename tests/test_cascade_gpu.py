@@ -71,6 +71,8 @@ CASES = [
     (512, 1100, [700, 20], [1, 1], -1, 16),              # decode, chunked prefix
     (512, 150, [80, 31], [80, 31], 60, 16),
     (256, 90, [30, 17], [30, 5], -1, 4),                  # page size 4: the general kernel
+    (256, 333, [70, 140], [70, 33], 200, 32),             # tcgen05 path, one K box per page
+    (512, 205, [90, 45], [90, 45], -1, 8),                # tcgen05 path, four K boxes per part
 ]
 
 
