@@ -217,3 +217,28 @@ def test_device_second_layer_flags_and_skips_bad_page_ids():
     assert torch.isfinite(run.out[:20].float()).all()   # request 0 unaffected
     del snap
     run.close()
+
+
+def test_ring_and_segment_plans_update_in_place_and_survive_a_failed_update():
+    pages = np.arange(9, dtype=np.int32)
+    geo = (16, 8, 256, 16)
+    rc, plan = pg.pg_plan_paged_prefill_ring(None, 1, [0, 10], [0, 9], pages, [0], *geo, 100)
+    assert rc == pg.PG_OK
+    rc, _ = pg.pg_plan_paged_prefill_ring(plan, 1, [0, 40], [0, 9], pages, [700], *geo, 100)
+    assert rc == pg.PG_OK
+    i = plan.info()
+    assert (i.num_tokens, i.max_pos_end) == (40, 740)
+    # 9 x 16 = 144 slots < window 100 + 60 tokens, and positions wrap: refused, plan unchanged
+    rc, _ = pg.pg_plan_paged_prefill_ring(plan, 1, [0, 60], [0, 9], pages, [700], *geo, 100)
+    assert rc == pg.PG_ERR_COVERAGE
+    assert (plan.info().num_tokens, plan.info().max_pos_end) == (40, 740)
+    plan.close()
+    rc, seg = pg.pg_plan_paged_segment(None, 1, [0, 4], [0, 2], [3, 5], [16], [100], [128], *geo)
+    assert rc == pg.PG_OK
+    rc, _ = pg.pg_plan_paged_segment(seg, 1, [0, 4], [0, 2], [3, 5], [16], [172], [200], *geo)
+    assert rc == pg.PG_OK and seg.info().max_pos_end == 204
+    # keys [200, 232) would run past the step's last position 203: refused, plan unchanged
+    rc, _ = pg.pg_plan_paged_segment(seg, 1, [0, 4], [0, 2], [3, 5], [16], [200], [200], *geo)
+    assert rc == pg.PG_ERR_COVERAGE
+    assert seg.info().max_pos_end == 204
+    seg.close()
