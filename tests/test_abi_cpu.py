@@ -155,3 +155,20 @@ def test_headers_are_plain_c():
                             "-fsyntax-only", "-"], input=f'#include "{h}"\n', text=True,
                            capture_output=True)
         assert r.returncode == 0, (h, r.stderr)
+
+
+def test_the_boundary_links_and_runs_from_plain_c(tmp_path):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    libdir = os.path.dirname(os.path.abspath(pg._lib._name))
+    exe = str(tmp_path / "abi_smoke")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", f"-I{INCLUDE}",
+                        os.path.join(here, "abi_smoke.c"), "-o", exe, f"-L{libdir}", "-lpg",
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and "c abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
