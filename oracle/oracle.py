@@ -124,18 +124,23 @@ def token_request_and_position(qo_indptr, start_pos):
     return req, start_pos[req] + local
 
 
-def slot_of(req, pos, kv_page_indptr, page_ids, page_size: int, ring: bool = False):
+def slot_of(req, pos, kv_page_indptr, page_ids, page_size: int, ring: bool = False,
+            kv_start=None):
     """(physical page id, in-page slot) holding KV position ``pos`` of ``req``.
 
     With ``ring`` the request's pages form a ring ("serving prep needs pool-write forms",
     Proposed Plan: window-crossing callers need a separate slot mapping): logical page
     pos // page_size lives in the request's page (pos // page_size) mod (pages held), so a
     position reuses the slot of the position one ring length (pages x page_size) earlier.
+    With ``kv_start`` (key segments) position kv_start_r + i lives in slot i of the request's
+    pages: the index counts from the segment's first position.
     """
     kv_page_indptr = np.asarray(kv_page_indptr, dtype=np.int64)
     page_ids = np.asarray(page_ids, dtype=np.int64)
     req = np.asarray(req, dtype=np.int64)
     pos = np.asarray(pos, dtype=np.int64)
+    if kv_start is not None:
+        pos = pos - np.asarray(kv_start, dtype=np.int64)[req]
     logical = pos // page_size
     if ring:
         logical = logical % (kv_page_indptr[req + 1] - kv_page_indptr[req])
@@ -185,9 +190,9 @@ def prep_hd512(q_raw, k_raw, w_q, w_k, eps, positions, theta):
 
 
 def prep_pool_writes(req, pos, kv_page_indptr, page_ids, page_size, layer, num_pages,
-                     num_kv_heads, head_dim, ring: bool = False):
+                     num_kv_heads, head_dim, ring: bool = False, kv_start=None):
     """Element offsets [T, 2, Hkv] of the K and V rows each token writes."""
-    page, slot = slot_of(req, pos, kv_page_indptr, page_ids, page_size, ring)
+    page, slot = slot_of(req, pos, kv_page_indptr, page_ids, page_size, ring, kv_start)
     kv = np.arange(2, dtype=np.int64)[None, :, None]
     head = np.arange(num_kv_heads, dtype=np.int64)[None, None, :]
     return pool_row_offset(layer, page[:, None, None], kv, head, slot[:, None, None],

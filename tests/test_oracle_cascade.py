@@ -132,3 +132,24 @@ def test_merge_states_algebra():
     assert np.allclose(l1, np.logaddexp(la, lb), atol=1e-14)
     o, l = O.merge_states(*zero, *zero)
     assert (o == 0).all() and np.isneginf(l).all()
+
+
+def test_segment_slots_follow_the_page_walk_from_the_segment_start():
+    # position kv_start + i lives in the i-th slot of the request's pages
+    rng = np.random.Generator(np.random.PCG64(23))
+    ps = 4
+    ci = W.make_cascade(rng, 13, [9, 22], [9, 5], ps, 2, 1, 8)
+    s = ci.suffix
+    req, pos = O.token_request_and_position(s.qo_indptr, s.start_pos)
+    page, slot = O.slot_of(req, pos, s.kv_page_indptr, s.page_ids, ps, kv_start=np.full(2, 13))
+    for t in range(len(pos)):
+        r = int(req[t])
+        pages = s.page_ids[s.kv_page_indptr[r]:s.kv_page_indptr[r + 1]]
+        walk = brute.slots_for_request(pages, int(pos[t]) - 13 + 1, ps)
+        assert (int(page[t]), int(slot[t])) == walk[-1]
+    # a segment starting at 0 is the linear mapping
+    f = ci.full
+    req, pos = O.token_request_and_position(f.qo_indptr, f.start_pos)
+    a = O.slot_of(req, pos, f.kv_page_indptr, f.page_ids, ps, kv_start=np.zeros(2, np.int64))
+    b = O.slot_of(req, pos, f.kv_page_indptr, f.page_ids, ps)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
