@@ -359,6 +359,18 @@ int pg_device_status(pg_stream_t stream);
 /* Kernels this library has launched since it was loaded (all devices). */
 int64_t pg_launch_count(void);
 
+/*
+ * Test hook for the kernels' bounded waits (failure detection without a GPU fault). With
+ * withhold = 1, every later prefill attention launch on the tensor-core path has the leading
+ * CTA of each pair skip the first key-tile arrival it owes (no copy is issued for that tile),
+ * and every bounded wait of those launches gives up after wait_limit_ns (in [1e6, 2e9]): the
+ * call's kernels then return with PG_ERR_DEVICE_TIMEOUT in the status word
+ * (pg_device_status) and their outputs are not valid; the context stays usable. withhold = 0
+ * restores normal launches and the two-second limit (wait_limit_ns is ignored). Process-wide;
+ * not for use while other threads launch. Errors: PG_ERR_ARG.
+ */
+int pg_test_bounded_wait(int32_t withhold, int64_t wait_limit_ns);
+
 /* Static text for a status code. */
 const char* pg_status_string(int status);
 

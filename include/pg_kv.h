@@ -7,11 +7,20 @@
  * count as the exact frontier account, nothing changing state before a step is admissible,
  * page ids meaningful only against the pool that issued them, and the path failing closed
  * at the sliding window (cache slots equal positions only below it). Verification: a forced
- * partial failure leaves both pools at their pre-request occupancy.
+ * partial failure leaves both pools at their pre-request occupancy. Review finding "Commit KV
+ * frontiers only after a successful step": admission only reserves; the frontier moves when
+ * the caller commits the step after its plan, copies and launches succeeded, and a step that
+ * failed anywhere after admission is aborted, returning its pages with the frontier unchanged,
+ * so a retry of the same step writes the same positions.
+ *
+ * Step life cycle per request: pg_kv_admit_step (pages reserved, step pending) ->
+ * pg_kv_batch_plan_inputs (plan inputs covering the pending step) -> prep / attention ->
+ * pg_kv_commit_step on success, or pg_kv_abort_step on any failure. A request holds at most
+ * one pending step.
  *
  * This is host code only (no CUDA calls, no device memory). A server owns two page
  * allocators, one per family; each request holds a state in both: its page list and its
- * frontier (the number of KV positions written, the same in both families). The page lists
+ * frontier (the number of KV positions committed, the same in both families). The page lists
  * feed pg_plan_paged_prefill's kv_page_indptr / page_ids / last_page_len / start_pos; a ring
  * server (pg_kv_server_create_ring) keeps the local family on a ring of pages past the window
  * instead of failing closed, for pg_plan_paged_prefill_ring.
@@ -40,7 +49,9 @@ enum {
   PG_KV_ERR_FOREIGN = -105,   /* the request id was not issued by this server, or is closed  */
   PG_KV_ERR_FRONTIER = -106,  /* a request's families disagree on the frontier, or a family
                                  holds other than the pages its frontier accounts for        */
-  PG_KV_ERR_CAPACITY = -107   /* a caller buffer is too small                                */
+  PG_KV_ERR_CAPACITY = -107,  /* a caller buffer is too small                                */
+  PG_KV_ERR_PENDING = -108    /* admit with a step already pending, or commit / abort / plan
+                                 inputs with no step pending                                 */
 };
 
 enum { PG_KV_LOCAL = 0, PG_KV_GLOBAL = 1 };  /* the two families: hd256 local, hd512 global */
@@ -77,14 +88,31 @@ int pg_kv_request_close(pg_kv_server_t srv, int64_t request_id);
  * The page count per family is the exact frontier account: ceil((frontier + n_tokens) /
  * page_size) (capped at the ring for the local family of a ring server) minus the pages the
  * family already holds. Before anything changes, the request
- * must belong to this server, both families must sit at the same frontier and hold exactly the
- * pages it accounts for, and the window and rotary bounds must hold. Then both families'
- * pages are reserved; if either pool refuses, the other reservation is dropped and
- * PG_KV_ERR_NO_PAGES returned, with both pools at their pre-request occupancy. Only when both
- * reservations stand are they committed and the frontier advanced. */
+ * must belong to this server, have no step pending (PG_KV_ERR_PENDING), both families must
+ * sit at the same frontier and hold exactly the pages it accounts for, and the window and
+ * rotary bounds must hold. Then both families' pages are reserved; if either pool refuses, the
+ * other reservation is dropped and PG_KV_ERR_NO_PAGES returned, with both pools at their
+ * pre-request occupancy. When both reservations stand, the request holds them and the step is
+ * pending: the frontier does not move until pg_kv_commit_step. */
 int pg_kv_admit_step(pg_kv_server_t srv, int64_t request_id, int32_t n_tokens);
 
-/* A request's frontier (positions written) and, per family, its page count. */
+/* Commit the request's pending step once its plan, copies and launches have all succeeded:
+ * the frontier advances by the step's tokens in both families. PG_KV_ERR_PENDING when no
+ * step is pending; nothing changes on any error. */
+int pg_kv_commit_step(pg_kv_server_t srv, int64_t request_id);
+
+/* Abort the request's pending step (plan building, a copy, a launch or the step's tail failed
+ * after admission): the pages the step reserved return to both pools and the frontier stays,
+ * so the request is exactly as before pg_kv_admit_step and the step can be admitted again.
+ * Positions the failed step may already have written past the frontier are rewritten by the
+ * retry before any query reads them. PG_KV_ERR_PENDING when no step is pending. */
+int pg_kv_abort_step(pg_kv_server_t srv, int64_t request_id);
+
+/* Tokens of the request's pending step (0: none). */
+int pg_kv_request_pending(pg_kv_server_t srv, int64_t request_id, int32_t* pending);
+
+/* A request's frontier (positions committed) and, per family, its page count (a pending
+ * step's pages included). */
 int pg_kv_request_info(pg_kv_server_t srv, int64_t request_id, int32_t* frontier,
                        int32_t* pages_local, int32_t* pages_global);
 
@@ -100,12 +128,13 @@ int pg_kv_free_pages(pg_kv_server_t srv, int32_t family, int32_t* n);
  * reservations in `family` are refused as if that pool were full. */
 int pg_kv_inject_refusal(pg_kv_server_t srv, int32_t family, int32_t count);
 
-/* Plan inputs of a batch for one family, after each request's admitted step of step_tokens[i]
- * tokens: kv_page_indptr [n + 1], page_ids (cap entries, in position order, or ring order for a
- * ring server's local family), last_page_len [n] (the frontier's slot count in its page),
- * start_pos [n]
- * (= frontier - step_tokens[i]), in the layout pg_plan_paged_prefill reads. Each step must be
- * no longer than the request's frontier. *n_page_ids receives the page-id count. */
+/* Plan inputs of a batch for one family, covering each request's pending step of
+ * step_tokens[i] tokens (which must equal the pending count: PG_KV_ERR_ARG otherwise;
+ * PG_KV_ERR_PENDING when a request has no step pending): kv_page_indptr [n + 1], page_ids
+ * (cap entries, in position order, or ring order for a ring server's local family),
+ * last_page_len [n] (slots used in the page of the step's last position), start_pos [n]
+ * (= the committed frontier), in the layout pg_plan_paged_prefill reads. *n_page_ids
+ * receives the page-id count. */
 int pg_kv_batch_plan_inputs(pg_kv_server_t srv, int32_t family, int32_t n,
                             const int64_t* request_ids, const int32_t* step_tokens,
                             int64_t* kv_page_indptr, int32_t* page_ids, int32_t cap,

@@ -447,17 +447,15 @@ using Dec512 = Cfg<512, 16, 32, 1, 2, true, 3>;
 
 template <class C>
 cudaError_t launch_split(const AttnArgs& a, dim3 grid, cudaStream_t stream) {
-  static bool configured[128] = {false};  // the shared-memory opt-in is per device
-  int dev = 0;
+  static PerDeviceOnce setup;  // the shared-memory opt-in, once per device
+  int dev = 0, unused = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_split_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::SMEM);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  e = setup.get(dev, [](int*) {
+    return cudaFuncSetAttribute(attn_split_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)C::SMEM);
+  }, &unused);
+  if (e != cudaSuccess) return e;
   attn_split_kernel<C><<<grid, kThreads, C::SMEM, stream>>>(a);
   count_launch();
   return cudaGetLastError();

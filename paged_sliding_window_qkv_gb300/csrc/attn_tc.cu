@@ -36,8 +36,9 @@
 // O holds 256 output columns: for head_dim 512 each query tile is two units, each computing
 // the full 512-wide S and half of O. The TMEM map is described at TcCfg.
 //
-// Every wait is bounded (two seconds of %globaltimer); a wait that runs out sets the
-// device status word, makes the CTA drain and free its tensor memory, and return.
+// Every wait is bounded (two seconds of %globaltimer unless the launch passes a shorter limit);
+// a wait that runs out sets the device status word, makes the CTA drain and free its tensor
+// memory, and return.
 #include "pg_internal.h"
 
 #include <cuda.h>
@@ -62,7 +63,6 @@ constexpr int kThreadsTc = 384;  // K producer 0; QK issuer 1; softmax 2..9; V p
 // the same relative precision, and O / l does not depend on the reference.
 constexpr float kRescaleLog2 = 48.f;
 constexpr float kHeadroomLog2 = 64.f;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // The kernel runs on clusters of two CTAs and issues its MMAs in the 2-SM form
 // (tcgen05 cta_group::2, M = 256): CTA c of the pair owns query tile c of a pair of adjacent
@@ -109,6 +109,16 @@ struct TcArgs {
   float scale_log2;
   float* lse;  // optional [T][Hq] natural-log normaliser of each row (null: not written)
   int* status;
+  uint64_t wait_ns;       // limit of every bounded wait
+  int32_t test_withhold;  // test hook: the leader's K producer withholds its first arrival
+};
+
+// What a bounded wait needs: the CTA's abort flag (set by whichever role gives up first), the
+// device status word, and the limit.
+struct WaitCtx {
+  volatile int* abort_flag;
+  int* status;
+  uint64_t limit_ns;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -142,29 +152,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait on the phase of the given parity. Returns false when the CTA is aborting
 // (another role gave up) or when this wait itself runs out of time.
-__device__ __forceinline__ bool mbar_wait_body(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, int* status) {
+__device__ __forceinline__ bool mbar_wait_body(uint32_t bar, uint32_t parity, const WaitCtx& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     // plain try_wait: with an explicit suspend-time hint, waiters woke measurably later
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      atomicOr(status, kStatusTimeout);
-      *abort_flag = 1;
+    if (*w.abort_flag) return false;
+    if (globaltimer() - t0 > w.limit_ns) {
+      atomicOr(w.status, kStatusTimeout);
+      *w.abort_flag = 1;
       return false;
     }
   }
 }
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       int* status) {
-  return mbar_wait_body(bar, parity, abort_flag, status);
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx w) {
+  return mbar_wait_body(bar, parity, w);
 }
 // The same wait inlined, for the MMA-issuing warps.
-__device__ __forceinline__ bool mbar_wait_inline(uint32_t bar, uint32_t parity,
-                                                 volatile int* abort_flag, int* status) {
-  return mbar_wait_body(bar, parity, abort_flag, status);
+__device__ __forceinline__ bool mbar_wait_inline(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  return mbar_wait_body(bar, parity, w);
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -410,6 +417,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint32_t* tmem_slot =
       reinterpret_cast<uint32_t*>(gbase + C::SMEM_DATA + C::XL_BYTES + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtx wc{abort_flag, a.status, a.wait_ns};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
@@ -500,7 +508,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // Q columns [256,512) of this CTA's tile, once the previous unit's QK MMAs have read them
         int go = 1;
         if (lane == 0) {
-          if (ui > 0 && !mbar_wait(QFREE, (ui - 1) & 1, abort_flag, a.status)) {
+          if (ui > 0 && !mbar_wait(QFREE, (ui - 1) & 1, wc)) {
             go = 0;
           } else {
             mbar_expect_tx_cl_relaxed(LEAD(QFULL), u.ntok > 0 ? (uint32_t)C::QS_BYTES : 0u);
@@ -555,6 +563,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                         head_rows + ((ks - u.kv_start) & (ps - 1)))
                         : 0;
         }
+        // test hook: the leader's K producer issues neither the arrival nor the copies of its
+        // first tile, so the QK issuer's wait on that slot runs out
+        if (!is_v && leader && a.test_withhold && ui == 0 && t == 0) continue;
         const int sh = tb * nbox;
         const bool fix = ((bm_fix >> sh) & box_mask) != 0u;
         const uint32_t bytes = (uint32_t)__popc((bm_load >> sh) & box_mask) * box_bytes;
@@ -568,8 +579,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           int r = 1;
           if (lane == 0) {
             for (int pp = 0; r && pp < KP; ++pp)
-              r = mbar_wait_inline(EMPTY(KSLOT(JJ, pp)), (KROUND(JJ, pp) & 1) ^ 1, abort_flag,
-                                   a.status) ? 1 : 0;
+              r = mbar_wait_inline(EMPTY(KSLOT(JJ, pp)), (KROUND(JJ, pp) & 1) ^ 1, wc) ? 1 : 0;
             if (r)
               for (int pp = 0; pp < KP; ++pp) mbar_expect_tx_cl_relaxed(LEAD(FULL(KSLOT(JJ, pp))), bytes);
           }
@@ -592,7 +602,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const int round = is_v ? (int)(JJ / NVR) : KROUND(JJ, pp);
           const int c0 = is_v ? u.dh * 4 + (int)rank * 2 : pp * 4;
           int r = 1;
-          if (lane == 0) r = mbar_wait_inline(EMPTY(s), (round & 1) ^ 1, abort_flag, a.status) ? 1 : 0;
+          if (lane == 0) r = mbar_wait_inline(EMPTY(s), (round & 1) ^ 1, wc) ? 1 : 0;
           if (!__shfl_sync(0xffffffffu, r, 0)) {
             ok = false;
             break;
@@ -610,7 +620,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
           if (fix) {
             if (bytes > 0) {
-              if (!__all_sync(0xffffffffu, mbar_wait(FIX, fix_phase, abort_flag, a.status))) {
+              if (!__all_sync(0xffffffffu, mbar_wait(FIX, fix_phase, wc))) {
                 ok = false;
                 break;
               }
@@ -654,7 +664,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr uint32_t IDESC_QK = idesc_bf16(2 * kM, kBN, false);
     constexpr uint32_t IDESC_PV = idesc_bf16(2 * kM, kDV, true);
     auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
-      const bool r = lane == 0 ? mbar_wait_inline(bar, parity, abort_flag, a.status) : false;
+      const bool r = lane == 0 ? mbar_wait_inline(bar, parity, wc) : false;
       return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
     };
     bool ok = true;
@@ -796,7 +806,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int32_t j = 0; ok && j < ntiles; ++j) {
         const int32_t JJ = J + j;
         const int b = JJ % NSB;
-        if (!__all_sync(0xffffffffu, mbar_wait_inline(SFULL + 8 * b, (JJ / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait_inline(SFULL + 8 * b, (JJ / NSB) & 1, wc))) { ok = false; break; }
         tc_fence_after();
         // both warps of the pair read the whole 64-key row: the row maximum needs no exchange
         uint32_t sv[kBN];
@@ -852,7 +862,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           const int32_t jp = JJ - 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, wc))) { ok = false; break; }
           tc_fence_after();
           for (int c = 0; c < kDV / 64; ++c) {
             uint32_t o[32];
@@ -878,10 +888,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         // P buffer JJ mod NPB is free once PV(JJ - NPB) has read it
         if (C::NPB == 2) {
-          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ / NSB) & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ / NSB) & 1) ^ 1, wc))) { ok = false; break; }
         } else if (JJ > 0) {
           const int32_t jp = JJ - 1;
-          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, abort_flag, a.status))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, wc))) { ok = false; break; }
         }
         {
           // this row's 32 keys: four 16-byte chunks h*4 .. h*4+3 of its 128-byte row, at
@@ -907,7 +917,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       if (ntiles > 0) {
         const int32_t jl = J + ntiles - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, abort_flag, a.status));
+        ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, wc));
         // the row sum is the sum of both halves' partial sums, swapped through shared memory.
         // The partner has read this unit's value before this warp writes the next one: that
         // write waits for the next unit's last PV, which needs the partner's P of that tile,
@@ -916,7 +926,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           xl[h * kM + row] = l;
           __syncwarp();
           if (lane == 0) mbar_arrive(pair_bar);
-          ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, abort_flag, a.status));
+          ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, wc));
           pair_phase ^= 1u;
           if (ok) l = xl[row] + xl[kM + row];
         }
@@ -969,9 +979,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   if (warp == 1 && lane == 0) {
     // every MMA of the pair has completed once the leader's final commits have arrived (in
-    // both CTAs)
+    // both CTAs); a wait that runs out is reported like any other
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(DRAIN, 0) && globaltimer() - t0 < kWaitLimitNs) {
+    while (!mbar_try_wait(DRAIN, 0)) {
+      if (globaltimer() - t0 > a.wait_ns) {
+        atomicOr(a.status, kStatusTimeout);
+        break;
+      }
     }
   }
   __syncthreads();
@@ -1069,27 +1083,29 @@ cudaError_t launch_tc(const AttnArgs& a, cudaStream_t stream) {
   t.scale_log2 = a.sm_scale_log2;
   t.lse = a.lse;
   t.status = a.status;
+  t.wait_ns = a.wait_ns;
+  t.test_withhold = a.test_withhold;
 
-  static int sms[128] = {0};  // the shared-memory opt-in and the SM count, per device
-  int dev = 0;
+  // the shared-memory opt-in and the SM count, once per device
+  static PerDeviceOnce setup;
+  int dev = 0, nsm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  if (!sms[dev]) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TcCfg<DQK>::SMEM);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sms[dev] = n > 0 ? n : 1;
-  }
+  e = setup.get(dev, [dev](int* n) {
+    cudaError_t r = cudaFuncSetAttribute(attn_tc_kernel<DQK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<DQK>::SMEM);
+    if (r != cudaSuccess) return r;
+    r = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+    if (*n < 1) *n = 1;
+    return r;
+  }, &nsm);
+  if (e != cudaSuccess) return e;
   // one persistent CTA per SM (its shared and tensor memory fill the SM), in clusters of two;
   // cluster i walks the units (pair of query tiles, KV head, 256-column output part) of its
   // rounds
   const int64_t units = (int64_t)a.plan.num_pairs * a.pool.num_kv_heads * (DQK / kDV);
   if (units == 0) return cudaSuccess;
-  const int64_t clusters = std::min<int64_t>(units, sms[dev] / 2 > 0 ? sms[dev] / 2 : 1);
+  const int64_t clusters = std::min<int64_t>(units, nsm / 2 > 0 ? nsm / 2 : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
   cfg.blockDim = dim3(kThreadsTc, 1, 1);

@@ -20,6 +20,15 @@ namespace pg {
 static std::atomic<int64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Bounded waits give up after two seconds unless the test hook set a shorter limit.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+static std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+static std::atomic<int32_t> g_test_withhold{0};
+void wait_settings(uint64_t* wait_ns, int32_t* test_withhold) {
+  *wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  *test_withhold = g_test_withhold.load(std::memory_order_relaxed);
+}
+
 // One status word per device, allocated on first use with that device current.
 static std::mutex g_status_mu;
 static int* g_status_dev[128] = {nullptr};
@@ -433,6 +442,7 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
   a.kv_chunk = plan->kv_chunk;
   a.max_chunks = plan->max_chunks;
   a.status = st;
+  wait_settings(&a.wait_ns, &a.test_withhold);
   cudaError_t e;
   if (plan->decode) {
     const size_t rows = (size_t)plan->num_req * plan->num_qo_heads * plan->max_chunks;
@@ -695,6 +705,7 @@ int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, in
   a.kv_chunk = plan->kv_chunk;
   a.max_chunks = plan->max_chunks;
   a.status = st;
+  wait_settings(&a.wait_ns, &a.test_withhold);
   return launch_attn_decode_static(a, D, s) == cudaSuccess ? PG_OK : PG_ERR_CUDA;
 }
 
@@ -713,6 +724,19 @@ int pg_device_status(pg_stream_t stream) {
 }
 
 int64_t pg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int pg_test_bounded_wait(int32_t withhold, int64_t wait_limit_ns) {
+  if (withhold == 0) {
+    g_test_withhold.store(0, std::memory_order_relaxed);
+    g_wait_ns.store(kDefaultWaitNs, std::memory_order_relaxed);
+    return PG_OK;
+  }
+  if (withhold != 1 || wait_limit_ns < 1000000 || wait_limit_ns > (int64_t)kDefaultWaitNs)
+    return PG_ERR_ARG;
+  g_wait_ns.store((uint64_t)wait_limit_ns, std::memory_order_relaxed);
+  g_test_withhold.store(1, std::memory_order_relaxed);
+  return PG_OK;
+}
 
 const char* pg_status_string(int s) {
   switch (s) {

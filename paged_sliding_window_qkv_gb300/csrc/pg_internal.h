@@ -5,7 +5,26 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace pg {
+
+// One-time, per-device set-up of a kernel's launch attributes (shared-memory opt-in, SM
+// count): the attributes belong to the whole process on each device, so the first caller on a
+// device runs `fn` once under std::call_once and every thread then reads the recorded result.
+// Devices 0..127.
+struct PerDeviceOnce {
+  std::once_flag flag[128];
+  cudaError_t err[128] = {};
+  int value[128] = {};
+  template <class F>
+  cudaError_t get(int dev, F fn, int* out) {
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::call_once(flag[dev], [&] { err[dev] = fn(&value[dev]); });
+    *out = value[dev];
+    return err[dev];
+  }
+};
 
 // Device view of a plan's metadata (all int32, uploaded by the plan builder).
 struct PlanDev {
@@ -70,7 +89,12 @@ struct AttnArgs {
   int32_t kv_chunk;     // keys per decode chunk
   int32_t max_chunks;
   int* status;
+  uint64_t wait_ns;       // limit of the kernels' bounded waits (nanoseconds)
+  int32_t test_withhold;  // test hook of pg_test_bounded_wait (0: off)
 };
+
+// Bounded-wait settings for the next launches: the default limit, or the test hook's.
+void wait_settings(uint64_t* wait_ns, int32_t* test_withhold);
 
 // Device status word: set by kernels that skip an out-of-range access.
 constexpr int kStatusBounds = 1;

@@ -1,8 +1,11 @@
 // Host-side page accounting for two-family paged KV serving ("feat(gemma4): paged KV serving
-// across both attention families", Description and Verification): one page allocator per
-// family, a per-request state in both, admission atomic across both pools with the page count
-// as the exact frontier account, every check before any state changes, and the local family
-// failing closed at its sliding window. Declared in include/pg_kv.h.
+// across both attention families", Description, Verification and the review finding "Commit KV
+// frontiers only after a successful step"): one page allocator per family, a per-request state
+// in both, admission atomic across both pools with the page count as the exact frontier
+// account, every check before any state changes, the local family failing closed at its
+// sliding window, and a step's frontier advanced only when the caller commits the step after
+// its launches succeeded (an aborted step returns its pages and leaves the frontier).
+// Declared in include/pg_kv.h.
 #include "../../include/pg_kv.h"
 
 #include <cstdint>
@@ -14,8 +17,10 @@
 namespace {
 
 struct KvRequest {
-  int32_t frontier[2] = {0, 0};     // positions written, per family (kept equal)
-  std::vector<int32_t> pages[2];    // page ids in position order, per family
+  int32_t frontier[2] = {0, 0};     // positions committed, per family (kept equal)
+  std::vector<int32_t> pages[2];    // page ids in position order, per family (pending included)
+  int32_t pending = 0;              // tokens of the admitted, not yet committed step (0: none)
+  int32_t pending_new[2] = {0, 0};  // pages that step took, per family (the tail of pages[f])
 };
 
 int32_t pages_for(int64_t len, int32_t ps) { return (int32_t)((len + ps - 1) / ps); }
@@ -56,11 +61,14 @@ struct pg_kv_server {
     const int32_t n = pages_for(frontier, page_size);
     return (family == PG_KV_LOCAL && ring_pages > 0 && n > ring_pages) ? ring_pages : n;
   }
-  // The frontier account: both families at one frontier, each holding exactly its pages.
+  // The frontier account: both families at one frontier, each holding exactly the pages of
+  // the frontier plus its pending step.
   bool consistent(const KvRequest& r) const {
-    if (r.frontier[0] != r.frontier[1]) return false;
-    for (int f = 0; f < 2; ++f)
-      if ((int64_t)r.pages[f].size() != held_for(f, r.frontier[f])) return false;
+    if (r.frontier[0] != r.frontier[1] || r.pending < 0) return false;
+    for (int f = 0; f < 2; ++f) {
+      if ((int64_t)r.pages[f].size() != held_for(f, (int64_t)r.frontier[f] + r.pending)) return false;
+      if (r.pending_new[f] < 0 || r.pending_new[f] > (int32_t)r.pages[f].size()) return false;
+    }
     return true;
   }
 };
@@ -124,6 +132,7 @@ int pg_kv_admit_step(pg_kv_server_t srv, int64_t request_id, int32_t n_tokens) {
   if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
   KvRequest& r = it->second;
   // every check before anything changes
+  if (r.pending != 0) return PG_KV_ERR_PENDING;
   if (!srv->consistent(r)) return PG_KV_ERR_FRONTIER;
   const int64_t len = (int64_t)r.frontier[0] + n_tokens;
   if (len > INT32_MAX) return PG_KV_ERR_ARG;
@@ -133,17 +142,53 @@ int pg_kv_admit_step(pg_kv_server_t srv, int64_t request_id, int32_t n_tokens) {
   if (len > srv->rope_rows) return PG_KV_ERR_ROPE;
   int32_t need[2];
   for (int f = 0; f < 2; ++f) need[f] = srv->held_for(f, len) - (int32_t)r.pages[f].size();
-  // reserve both before committing either; a refused side drops the other
+  // reserve both before recording either; a refused side drops the other
   std::vector<int32_t> got[2];
   if (!srv->reserve(PG_KV_LOCAL, need[PG_KV_LOCAL], &got[PG_KV_LOCAL])) return PG_KV_ERR_NO_PAGES;
   if (!srv->reserve(PG_KV_GLOBAL, need[PG_KV_GLOBAL], &got[PG_KV_GLOBAL])) {
     srv->give_back(PG_KV_LOCAL, got[PG_KV_LOCAL]);
     return PG_KV_ERR_NO_PAGES;
   }
+  // the step is pending: its pages are held, the frontier stays until pg_kv_commit_step
   for (int f = 0; f < 2; ++f) {
     r.pages[f].insert(r.pages[f].end(), got[f].begin(), got[f].end());
-    r.frontier[f] = (int32_t)len;
+    r.pending_new[f] = (int32_t)got[f].size();
   }
+  r.pending = n_tokens;
+  return PG_KV_OK;
+}
+
+int pg_kv_commit_step(pg_kv_server_t srv, int64_t request_id) {
+  if (!srv) return PG_KV_ERR_ARG;
+  auto it = srv->requests.find(request_id);
+  if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
+  KvRequest& r = it->second;
+  if (r.pending == 0) return PG_KV_ERR_PENDING;
+  if (!srv->consistent(r)) return PG_KV_ERR_FRONTIER;
+  for (int f = 0; f < 2; ++f) {
+    r.frontier[f] += r.pending;
+    r.pending_new[f] = 0;
+  }
+  r.pending = 0;
+  return PG_KV_OK;
+}
+
+int pg_kv_abort_step(pg_kv_server_t srv, int64_t request_id) {
+  if (!srv) return PG_KV_ERR_ARG;
+  auto it = srv->requests.find(request_id);
+  if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
+  KvRequest& r = it->second;
+  if (r.pending == 0) return PG_KV_ERR_PENDING;
+  if (!srv->consistent(r)) return PG_KV_ERR_FRONTIER;
+  // the step's own pages go back to their pools; the pages before it and the frontier stay
+  for (int f = 0; f < 2; ++f) {
+    const size_t keep = r.pages[f].size() - (size_t)r.pending_new[f];
+    std::vector<int32_t> back(r.pages[f].begin() + (std::ptrdiff_t)keep, r.pages[f].end());
+    r.pages[f].resize(keep);
+    srv->give_back(f, back);
+    r.pending_new[f] = 0;
+  }
+  r.pending = 0;
   return PG_KV_OK;
 }
 
@@ -155,6 +200,14 @@ int pg_kv_request_info(pg_kv_server_t srv, int64_t request_id, int32_t* frontier
   if (frontier) *frontier = it->second.frontier[0];
   if (pages_local) *pages_local = (int32_t)it->second.pages[PG_KV_LOCAL].size();
   if (pages_global) *pages_global = (int32_t)it->second.pages[PG_KV_GLOBAL].size();
+  return PG_KV_OK;
+}
+
+int pg_kv_request_pending(pg_kv_server_t srv, int64_t request_id, int32_t* pending) {
+  if (!srv || !pending) return PG_KV_ERR_ARG;
+  auto it = srv->requests.find(request_id);
+  if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
+  *pending = it->second.pending;
   return PG_KV_OK;
 }
 
@@ -200,7 +253,9 @@ int pg_kv_batch_plan_inputs(pg_kv_server_t srv, int32_t family, int32_t n,
     if (it == srv->requests.end()) return PG_KV_ERR_FOREIGN;
     const KvRequest& r = it->second;
     if (!srv->consistent(r)) return PG_KV_ERR_FRONTIER;
-    if (step_tokens[i] < 1 || step_tokens[i] > r.frontier[family]) return PG_KV_ERR_ARG;
+    // the plan covers the request's admitted step, which must still be pending
+    if (r.pending == 0) return PG_KV_ERR_PENDING;
+    if (step_tokens[i] != r.pending) return PG_KV_ERR_ARG;
     total += (int64_t)r.pages[family].size();
   }
   if (total > cap) return PG_KV_ERR_CAPACITY;
@@ -213,9 +268,10 @@ int pg_kv_batch_plan_inputs(pg_kv_server_t srv, int32_t family, int32_t n,
     for (size_t k = 0; k < p.size(); ++k) page_ids[off + (int64_t)k] = p[k];
     off += (int64_t)p.size();
     kv_page_indptr[i + 1] = off;
-    // the frontier's slot count in its page (a ring plan does not read it)
-    last_page_len[i] = r.frontier[family] - ((r.frontier[family] - 1) / srv->page_size) * srv->page_size;
-    start_pos[i] = (int64_t)r.frontier[family] - step_tokens[i];
+    // the step's last position's slot count in its page (a ring plan does not read it)
+    const int32_t end = r.frontier[family] + r.pending;
+    last_page_len[i] = end - ((end - 1) / srv->page_size) * srv->page_size;
+    start_pos[i] = (int64_t)r.frontier[family];
   }
   *n_page_ids = (int32_t)total;
   return PG_KV_OK;

@@ -414,17 +414,25 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   const int32_t nrows = a.num_qo_heads + (D == 256 ? 2 : 1) * a.pool.num_kv_heads;
   const uint32_t stage = (uint32_t)((((int64_t)nrows * D * 2 + D * 4 + 16) + 127) & ~(int64_t)127);
-  // the occupancy and the attribute depend only on the device and the stage size
-  static thread_local int cached_dev = -1;
-  static thread_local uint32_t cached_stage = 0;
-  static thread_local int sms = 0, per_sm = 0, nst = 0;
-  static thread_local size_t smem = 0;
-  int dev = 0;
+  // The shared-memory opt-in is set to the kernel's maximum once per device (it is a
+  // process-wide attribute); the stage count and occupancy depend on the device and the stage
+  // size and are cached per thread.
+  static PerDeviceOnce setup;
+  int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  e = setup.get(dev, [dev](int* n) {
+    cudaError_t r = cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (r != cudaSuccess) return r;
+    return cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+  }, &sms);
+  if (e != cudaSuccess) return e;
+  static thread_local int cached_dev = -1;
+  static thread_local uint32_t cached_stage = 0;
+  static thread_local int per_sm = 0, nst = 0;
+  static thread_local size_t smem = 0;
   if (dev != cached_dev || stage != cached_stage) {
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-      return e;
     int by_regs = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&by_regs, prep_kernel<D>, kPrepThreads,
                                                            0)) != cudaSuccess)
@@ -432,18 +440,18 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t stream) {
     if (by_regs < 1) by_regs = 1;
     if (by_regs > 4) by_regs = 4;
     constexpr uint32_t kSmBudget = 210 * 1024;
-    nst = (int)(kSmBudget / by_regs / stage);
-    if (nst < 2) nst = 2;
-    if (nst > 8) nst = 8;
-    smem = (size_t)((16 * nst + 4 + 127) & ~127) + (size_t)nst * stage;
-    if (smem > 227 * 1024) return cudaErrorInvalidValue;
-    if ((e = cudaFuncSetAttribute(prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem)) != cudaSuccess)
+    int n = (int)(kSmBudget / by_regs / stage);
+    if (n < 2) n = 2;
+    if (n > 8) n = 8;
+    const size_t sm_bytes = (size_t)((16 * n + 4 + 127) & ~127) + (size_t)n * stage;
+    if (sm_bytes > 227 * 1024) return cudaErrorInvalidValue;
+    int occ = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, prep_kernel<D>, kPrepThreads,
+                                                           sm_bytes)) != cudaSuccess)
       return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prep_kernel<D>, kPrepThreads,
-                                                           smem)) != cudaSuccess)
-      return e;
-    if (per_sm < 1) per_sm = 1;
+    per_sm = occ < 1 ? 1 : occ;
+    nst = n;
+    smem = sm_bytes;
     cached_dev = dev;
     cached_stage = stage;
   }

@@ -104,6 +104,7 @@ _attn_noalloc = _sig("pg_attn_paged_decode_noalloc", C.c_int, _P, C.POINTER(pg_p
 PG_NOALLOC_SCRATCH_BYTES = 32 << 20
 _devstat = _sig("pg_device_status", C.c_int, _P)
 _launches = _sig("pg_launch_count", _I64)
+_test_wait = _sig("pg_test_bounded_wait", C.c_int, _I32, _I64)
 _sstr = _sig("pg_status_string", C.c_char_p, C.c_int)
 
 
@@ -144,6 +145,12 @@ def pg_status_string(status: int) -> str:
 
 def pg_launch_count() -> int:
     return int(_launches())
+
+
+def pg_test_bounded_wait(withhold, wait_limit_ns=0) -> int:
+    """Test hook: withhold=1 makes later tensor-core prefill launches skip one key-tile
+    arrival and give up their bounded waits after wait_limit_ns; withhold=0 restores them."""
+    return int(_test_wait(int(withhold), int(wait_limit_ns)))
 
 
 def pg_device_status(stream=None) -> int:
@@ -321,7 +328,7 @@ EXPORTED = ["pg_plan_paged_prefill", "pg_plan_paged_prefill_ring", "pg_plan_page
             "pg_plan_destroy", "pg_plan_info", "pg_rope_table",
             "pg_prep_paged_hd256", "pg_prep_paged_hd512", "pg_workspace_bytes",
             "pg_attn_paged_prefill", "pg_attn_paged_prefill_hd512", "pg_device_status",
-            "pg_launch_count", "pg_status_string"]
+            "pg_launch_count", "pg_status_string", "pg_test_bounded_wait"]
 
 
 # ---------------------------------------------------------------- page accounting (include/pg_kv.h)
@@ -333,6 +340,7 @@ PG_KV_ERR_ROPE = -104
 PG_KV_ERR_FOREIGN = -105
 PG_KV_ERR_FRONTIER = -106
 PG_KV_ERR_CAPACITY = -107
+PG_KV_ERR_PENDING = -108
 PG_KV_LOCAL = 0
 PG_KV_GLOBAL = 1
 
@@ -344,6 +352,9 @@ _lib.pg_kv_server_destroy.restype = None
 _lib.pg_kv_request_open.argtypes = [C.c_void_p, _I64P]
 _lib.pg_kv_request_close.argtypes = [C.c_void_p, C.c_int64]
 _lib.pg_kv_admit_step.argtypes = [C.c_void_p, C.c_int64, C.c_int32]
+_lib.pg_kv_commit_step.argtypes = [C.c_void_p, C.c_int64]
+_lib.pg_kv_abort_step.argtypes = [C.c_void_p, C.c_int64]
+_lib.pg_kv_request_pending.argtypes = [C.c_void_p, C.c_int64, _I32P]
 _lib.pg_kv_request_info.argtypes = [C.c_void_p, C.c_int64, _I32P, _I32P, _I32P]
 _lib.pg_kv_request_pages.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_int32, _I32P]
 _lib.pg_kv_free_pages.argtypes = [C.c_void_p, C.c_int32, _I32P]
@@ -396,6 +407,21 @@ def pg_kv_admit_step(srv, request_id, n_tokens) -> int:
     return _lib.pg_kv_admit_step(srv, int(request_id), int(n_tokens))
 
 
+def pg_kv_commit_step(srv, request_id) -> int:
+    return _lib.pg_kv_commit_step(srv, int(request_id))
+
+
+def pg_kv_abort_step(srv, request_id) -> int:
+    return _lib.pg_kv_abort_step(srv, int(request_id))
+
+
+def pg_kv_request_pending(srv, request_id):
+    """Returns (status, tokens of the pending step, 0 when none)."""
+    n = C.c_int32()
+    rc = _lib.pg_kv_request_pending(srv, int(request_id), C.byref(n))
+    return rc, n.value
+
+
 def pg_kv_request_info(srv, request_id):
     """Returns (status, frontier, pages_local, pages_global)."""
     f, pl, pg_ = C.c_int32(), C.c_int32(), C.c_int32()
@@ -443,5 +469,6 @@ def pg_kv_batch_plan_inputs(srv, family, request_ids, step_tokens, cap=1 << 20):
 
 
 EXPORTED += ["pg_kv_server_create", "pg_kv_server_create_ring", "pg_kv_server_destroy", "pg_kv_request_open",
-             "pg_kv_request_close", "pg_kv_admit_step", "pg_kv_request_info", "pg_kv_request_pages",
+             "pg_kv_request_close", "pg_kv_admit_step", "pg_kv_commit_step", "pg_kv_abort_step",
+             "pg_kv_request_pending", "pg_kv_request_info", "pg_kv_request_pages",
              "pg_kv_free_pages", "pg_kv_inject_refusal", "pg_kv_batch_plan_inputs"]

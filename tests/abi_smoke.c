@@ -25,7 +25,12 @@ int main(void) {
   if (pg_kv_admit_step(srv, rid, 20) != PG_KV_OK) return 6;
   int32_t frontier = 0, nl = 0, ng = 0, nfree = 0;
   if (pg_kv_request_info(srv, rid, &frontier, &nl, &ng) != PG_KV_OK) return 7;
-  if (frontier != 20 || nl != 2 || ng != 2) return 8;
+  if (frontier != 0 || nl != 2 || ng != 2) return 8;  /* reserved, not committed */
+  if (pg_kv_abort_step(srv, rid) != PG_KV_OK) return 12;
+  if (pg_kv_free_pages(srv, PG_KV_LOCAL, &nfree) != PG_KV_OK || nfree != 4) return 13;
+  if (pg_kv_admit_step(srv, rid, 20) != PG_KV_OK || pg_kv_commit_step(srv, rid) != PG_KV_OK) return 14;
+  if (pg_kv_request_info(srv, rid, &frontier, &nl, &ng) != PG_KV_OK) return 15;
+  if (frontier != 20 || nl != 2 || ng != 2) return 16;
   if (pg_kv_admit_step(srv, rid, 100) != PG_KV_ERR_WINDOW) return 9; /* fails closed */
   if (pg_kv_request_close(srv, rid) != PG_KV_OK) return 10;
   if (pg_kv_free_pages(srv, PG_KV_LOCAL, &nfree) != PG_KV_OK || nfree != 4) return 11;

@@ -4,7 +4,9 @@ What is checked follows "feat(gemma4): paged KV serving across both attention fa
 Description and Verification: admission atomic across both pools, the page count as the exact
 frontier account, a forced partial failure leaving both pools at their pre-request occupancy,
 checks before any state change, page ids valid only against the issuing server, and failing
-closed at the sliding window.
+closed at the sliding window; and its review finding "Commit KV frontiers only after a
+successful step": admission reserves, the frontier moves only on commit, and an aborted step
+leaves both pools and the frontier as they were before admission.
 """
 import numpy as np
 import pytest
@@ -36,12 +38,20 @@ def open_req(s):
     return rid
 
 
+def step(s, rid, n):
+    """Admit a step and commit it (the step's launches succeeded); returns the admit status."""
+    rc = pg.pg_kv_admit_step(s, rid, n)
+    if rc == pg.PG_KV_OK:
+        assert pg.pg_kv_commit_step(s, rid) == pg.PG_KV_OK
+    return rc
+
+
 def test_page_count_is_the_exact_frontier_account():
     s = server(ps=16)
     rid = open_req(s)
     frontier = 0
     for n in [1, 15, 1, 16, 17, 3, 64, 1]:
-        assert pg.pg_kv_admit_step(s, rid, n) == pg.PG_KV_OK
+        assert step(s, rid, n) == pg.PG_KV_OK
         frontier += n
         f, nl, ng, _, _ = state(s, rid)
         assert f == frontier
@@ -55,14 +65,14 @@ def test_forced_partial_failure_leaves_both_pools_untouched():
     for refused in (G, L):
         s = server()
         rid = open_req(s)
-        assert pg.pg_kv_admit_step(s, rid, 20) == pg.PG_KV_OK
+        assert step(s, rid, 20) == pg.PG_KV_OK
         before_free, before_state = free(s), state(s, rid)
         assert pg.pg_kv_inject_refusal(s, refused, 1) == pg.PG_KV_OK
-        assert pg.pg_kv_admit_step(s, rid, 30) == pg.PG_KV_ERR_NO_PAGES
+        assert step(s, rid, 30) == pg.PG_KV_ERR_NO_PAGES
         assert free(s) == before_free
         assert state(s, rid) == before_state
         # the refusal was one-shot: the same step is admitted next
-        assert pg.pg_kv_admit_step(s, rid, 30) == pg.PG_KV_OK
+        assert step(s, rid, 30) == pg.PG_KV_OK
         assert state(s, rid)[0] == 50
         pg.pg_kv_server_destroy(s)
 
@@ -70,9 +80,9 @@ def test_forced_partial_failure_leaves_both_pools_untouched():
 def test_exhausted_family_refuses_without_stranding_the_other():
     s = server(pages_local=64, pages_global=3, ps=16)
     rid = open_req(s)
-    assert pg.pg_kv_admit_step(s, rid, 48) == pg.PG_KV_OK       # 3 pages each
+    assert step(s, rid, 48) == pg.PG_KV_OK       # 3 pages each
     before = free(s), state(s, rid)
-    assert pg.pg_kv_admit_step(s, rid, 1) == pg.PG_KV_ERR_NO_PAGES   # global has no 4th page
+    assert step(s, rid, 1) == pg.PG_KV_ERR_NO_PAGES   # global has no 4th page
     assert (free(s), state(s, rid)) == before
     assert free(s) == (61, 0)
     pg.pg_kv_server_destroy(s)
@@ -81,15 +91,15 @@ def test_exhausted_family_refuses_without_stranding_the_other():
 def test_window_fails_closed_and_rope_bound():
     s = server(window=31, fail_closed=1, rope_rows=40)
     rid = open_req(s)
-    assert pg.pg_kv_admit_step(s, rid, 32) == pg.PG_KV_OK        # window_left + 1 positions
+    assert step(s, rid, 32) == pg.PG_KV_OK        # window_left + 1 positions
     before = free(s), state(s, rid)
-    assert pg.pg_kv_admit_step(s, rid, 1) == pg.PG_KV_ERR_WINDOW
+    assert step(s, rid, 1) == pg.PG_KV_ERR_WINDOW
     assert (free(s), state(s, rid)) == before
     pg.pg_kv_server_destroy(s)
     s = server(window=31, fail_closed=0, rope_rows=40)
     rid = open_req(s)
-    assert pg.pg_kv_admit_step(s, rid, 40) == pg.PG_KV_OK        # positions 0..39 < rope_rows
-    assert pg.pg_kv_admit_step(s, rid, 1) == pg.PG_KV_ERR_ROPE
+    assert step(s, rid, 40) == pg.PG_KV_OK        # positions 0..39 < rope_rows
+    assert step(s, rid, 1) == pg.PG_KV_ERR_ROPE
     assert state(s, rid)[0] == 40
     pg.pg_kv_server_destroy(s)
 
@@ -97,14 +107,14 @@ def test_window_fails_closed_and_rope_bound():
 def test_foreign_and_closed_requests_are_refused():
     s1, s2 = server(), server()
     r1 = open_req(s1)
-    assert pg.pg_kv_admit_step(s2, r1 + 1000, 1) == pg.PG_KV_ERR_FOREIGN
-    assert pg.pg_kv_admit_step(s1, r1, 17) == pg.PG_KV_OK
+    assert step(s2, r1 + 1000, 1) == pg.PG_KV_ERR_FOREIGN
+    assert step(s1, r1, 17) == pg.PG_KV_OK
     assert free(s1) == (62, 62)
     assert pg.pg_kv_request_close(s1, r1) == pg.PG_KV_OK
     assert free(s1) == (64, 64)                                   # pages returned to both pools
-    assert pg.pg_kv_admit_step(s1, r1, 1) == pg.PG_KV_ERR_FOREIGN
+    assert step(s1, r1, 1) == pg.PG_KV_ERR_FOREIGN
     assert pg.pg_kv_request_close(s1, r1) == pg.PG_KV_ERR_FOREIGN
-    assert pg.pg_kv_admit_step(s1, 0, 1) == pg.PG_KV_ERR_FOREIGN
+    assert step(s1, 0, 1) == pg.PG_KV_ERR_FOREIGN
     for s in (s1, s2):
         pg.pg_kv_server_destroy(s)
 
@@ -114,9 +124,9 @@ def test_bad_arguments():
     assert pg.pg_kv_server_create(4, 4, 16, -1, 1, 100)[0] == pg.PG_KV_ERR_ARG
     s = server()
     rid = open_req(s)
-    assert pg.pg_kv_admit_step(s, rid, 0) == pg.PG_KV_ERR_ARG
+    assert step(s, rid, 0) == pg.PG_KV_ERR_ARG
     assert pg.pg_kv_free_pages(s, 2)[0] == pg.PG_KV_ERR_ARG
-    assert pg.pg_kv_admit_step(s, rid, 40) == pg.PG_KV_OK
+    assert step(s, rid, 40) == pg.PG_KV_OK
     assert pg.pg_kv_request_pages(s, rid, L, cap=2)[0] == pg.PG_KV_ERR_CAPACITY
     pg.pg_kv_server_destroy(s)
 
@@ -127,20 +137,22 @@ def test_batch_plan_inputs_follow_the_plan_contract():
     rids = [open_req(s) for _ in range(3)]
     lens = [5, 40, 16]
     for r, n in zip(rids, lens):
-        assert pg.pg_kv_admit_step(s, r, n) == pg.PG_KV_OK
-    # a decode step of one token each, then the plan inputs for the local family
+        assert step(s, r, n) == pg.PG_KV_OK
+    # without a pending step there is nothing to plan
+    assert pg.pg_kv_batch_plan_inputs(s, L, rids, [1, 1, 1])[0] == pg.PG_KV_ERR_PENDING
+    # a decode step of one token each is admitted (pending), then the local family's inputs
     for r in rids:
         assert pg.pg_kv_admit_step(s, r, 1) == pg.PG_KV_OK
     rc, indptr, pages, last, start = pg.pg_kv_batch_plan_inputs(s, L, rids, [1, 1, 1])
     assert rc == pg.PG_KV_OK
     kv_len = (np.diff(indptr) - 1) * ps + last
     assert (kv_len == np.array(lens) + 1).all()                    # coverage: kv_len = start + qo_len
-    assert (start + 1 == kv_len).all()
+    assert (start == np.array(lens)).all()                         # start = the committed frontier
     assert ((1 <= last) & (last <= ps)).all()
     assert len(set(pages.tolist())) == len(pages)                  # no page held twice
     for i, r in enumerate(rids):
         assert tuple(pages[indptr[i]:indptr[i + 1]]) == tuple(pg.pg_kv_request_pages(s, r, L)[1])
-    # a step longer than the frontier has no plan
+    # a step count other than the pending one has no plan
     assert pg.pg_kv_batch_plan_inputs(s, L, rids, [1, 1, 100])[0] == pg.PG_KV_ERR_ARG
     pg.pg_kv_server_destroy(s)
 
@@ -173,6 +185,11 @@ def test_random_traffic_keeps_the_books(ring):
             if rc != pg.PG_KV_OK:
                 assert rc == pg.PG_KV_ERR_NO_PAGES
                 assert (free(s), state(s, r)) == before
+            elif rng.random() < 0.3:       # the step failed after admission
+                assert pg.pg_kv_abort_step(s, r) == pg.PG_KV_OK
+                assert (free(s), state(s, r)) == before
+            else:
+                assert pg.pg_kv_commit_step(s, r) == pg.PG_KV_OK
             pg.pg_kv_inject_refusal(s, 0, 0)
             pg.pg_kv_inject_refusal(s, 1, 0)
         # conservation and exclusivity in both pools
@@ -196,7 +213,7 @@ def test_ring_server_caps_the_local_family_at_its_ring():
     rid = open_req(s)
     frontier = 0
     for n in [37, 20, 64, 1, 50, 64, 1, 64, 3, 64, 64]:
-        assert pg.pg_kv_admit_step(s, rid, n) == pg.PG_KV_OK
+        assert step(s, rid, n) == pg.PG_KV_OK
         frontier += n
         f, nl, ng, local, _ = state(s, rid)
         assert f == frontier
@@ -206,13 +223,14 @@ def test_ring_server_caps_the_local_family_at_its_ring():
     assert frontier > 2 * ring * ps                      # wrapped more than once
     # a step longer than the ring allows beside the window is refused, nothing changed
     before = free(s), state(s, rid)
-    assert pg.pg_kv_admit_step(s, rid, max_step + 1) == pg.PG_KV_ERR_WINDOW
+    assert step(s, rid, max_step + 1) == pg.PG_KV_ERR_WINDOW
     assert (free(s), state(s, rid)) == before
-    # plan inputs: the ring's pages in ring order, start = frontier - step
+    # plan inputs of a pending 3-token step: the ring's pages in ring order, start = frontier
+    assert pg.pg_kv_admit_step(s, rid, 3) == pg.PG_KV_OK
     rc, indptr, pages, last, start = pg.pg_kv_batch_plan_inputs(s, L, [rid], [3])
     assert rc == pg.PG_KV_OK
     assert tuple(pages) == state(s, rid)[3] and len(pages) == ring
-    assert start[0] == frontier - 3 and last[0] == (frontier - 1) % ps + 1
+    assert start[0] == frontier and last[0] == (frontier + 3 - 1) % ps + 1
     assert pg.pg_kv_request_close(s, rid) == pg.PG_KV_OK
     assert free(s) == (40, 64)
     pg.pg_kv_server_destroy(s)
@@ -222,3 +240,67 @@ def test_ring_server_rejects_bad_arguments():
     assert pg.pg_kv_server_create_ring(8, 8, 16, 100, 0, 1 << 20)[0] == pg.PG_KV_ERR_ARG
     assert pg.pg_kv_server_create_ring(8, 8, 0, 100, 8, 1 << 20)[0] == pg.PG_KV_ERR_ARG
     assert pg.pg_kv_server_create_ring(8, 8, 16, -1, 8, 1 << 20)[0] == pg.PG_KV_ERR_ARG
+
+
+def test_frontier_moves_only_on_commit():
+    ps = 16
+    s = server(ps=ps)
+    rid = open_req(s)
+    assert step(s, rid, 20) == pg.PG_KV_OK
+    assert pg.pg_kv_admit_step(s, rid, 30) == pg.PG_KV_OK
+    f, nl, ng, _, _ = state(s, rid)
+    assert f == 20 and nl == ng == -(-50 // ps)          # pages held, frontier not moved
+    assert pg.pg_kv_request_pending(s, rid) == (pg.PG_KV_OK, 30)
+    # one pending step at a time
+    before = free(s), state(s, rid)
+    assert pg.pg_kv_admit_step(s, rid, 1) == pg.PG_KV_ERR_PENDING
+    assert (free(s), state(s, rid)) == before
+    assert pg.pg_kv_commit_step(s, rid) == pg.PG_KV_OK
+    assert state(s, rid)[0] == 50
+    assert pg.pg_kv_request_pending(s, rid) == (pg.PG_KV_OK, 0)
+    # nothing pending: commit and abort are refused and change nothing
+    before = free(s), state(s, rid)
+    assert pg.pg_kv_commit_step(s, rid) == pg.PG_KV_ERR_PENDING
+    assert pg.pg_kv_abort_step(s, rid) == pg.PG_KV_ERR_PENDING
+    assert (free(s), state(s, rid)) == before
+    assert pg.pg_kv_commit_step(s, rid + 99) == pg.PG_KV_ERR_FOREIGN
+    assert pg.pg_kv_abort_step(s, rid + 99) == pg.PG_KV_ERR_FOREIGN
+    pg.pg_kv_server_destroy(s)
+
+
+@pytest.mark.parametrize("ring", [False, True], ids=["linear", "ring"])
+def test_aborted_step_restores_both_pools_and_the_frontier(ring):
+    # the review finding: a step that fails after admission (plan, copy, launch or tail) must not
+    # leave the frontier claiming its tokens, else a retry's start_pos skips them
+    ps = 16
+    if ring:
+        rc, s = pg.pg_kv_server_create_ring(40, 64, ps, 100, 64, 1 << 20)
+        assert rc == pg.PG_KV_OK
+        steps = [64, 64, 64, 40]                          # past the 11-page ring
+    else:
+        s = server(ps=ps)
+        steps = [37, 20]
+    rid = open_req(s)
+    for n in steps:
+        assert step(s, rid, n) == pg.PG_KV_OK
+    frontier = sum(steps)
+    before = free(s), state(s, rid)
+    rc0, ind0, pages0, last0, start0 = (None,) * 5
+    for attempt in range(3):
+        assert pg.pg_kv_admit_step(s, rid, 33) == pg.PG_KV_OK
+        rc, ind, pages, last, start = pg.pg_kv_batch_plan_inputs(s, L, [rid], [33])
+        assert rc == pg.PG_KV_OK and start[0] == frontier
+        if attempt == 0:
+            ind0, pages0, last0 = ind, pages, last
+        else:                                             # a retry plans the very same span
+            assert (ind == ind0).all() and (pages == pages0).all() and (last == last0).all()
+        if attempt < 2:
+            assert pg.pg_kv_abort_step(s, rid) == pg.PG_KV_OK
+            assert (free(s), state(s, rid)) == before
+    assert pg.pg_kv_commit_step(s, rid) == pg.PG_KV_OK
+    assert state(s, rid)[0] == frontier + 33
+    # closing a request with a pending step returns every page
+    assert pg.pg_kv_admit_step(s, rid, 5) == pg.PG_KV_OK
+    assert pg.pg_kv_request_close(s, rid) == pg.PG_KV_OK
+    assert free(s) == ((40, 64) if ring else (64, 64))
+    pg.pg_kv_server_destroy(s)

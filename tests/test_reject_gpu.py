@@ -199,24 +199,67 @@ def test_device_second_layer_flags_and_skips_bad_page_ids():
     run = _base_run()
     torch.cuda.synchronize()
     assert pg.pg_device_status() == pg.PG_OK
+    # The pool the calls see is the first 16 pages of an allocation of 16 + 8 pages, so the bad
+    # id planted below (a spare page) addresses memory this test owns even if a kernel's bounds
+    # check ever failed to hold; the spare pages must stay untouched.
+    n_pages, spare = run.pool.shape[1], 8
+    big = torch.full((1, n_pages + spare) + tuple(run.pool.shape[2:]), -1, dtype=torch.int16,
+                     device="cuda").view(torch.bfloat16)
+    run.pool = big[:, :n_pages]
+    assert run.pool.is_contiguous()
+    run.pool_desc = pg.pool_descriptor(run.pool)
+    assert run.pool_desc.num_pages == n_pages
     info = run.plan.info()
     # corrupt the device copy of the first page id of request 1 (host bounds stay valid)
     first = int(run.fi.batch.kv_page_indptr[1])
-    bad = np.array([run.pool_desc.num_pages + 1000], np.int32)
+    bad = np.array([n_pages + 3], np.int32)
     rt = _cudart()
     rt.cudaMemcpy.argtypes = [C.c_void_p, C.c_void_p, C.c_size_t, C.c_int]
     assert rt.cudaMemcpy(info.d_page_ids + 4 * first, bad.ctypes.data, 4, 1) == 0
-    snap = _snapshot(run)
     assert run.prep_status() == pg.PG_OK
     assert pg.pg_device_status() == pg.PG_ERR_DEVICE_BOUNDS
     assert pg.pg_device_status() == pg.PG_OK   # read-and-clear
-    # request 1's tokens were skipped: its first page (slots 0..15) stayed sentinel
     torch.cuda.synchronize()
     assert run.attn_status() == pg.PG_OK
     assert pg.pg_device_status() == pg.PG_ERR_DEVICE_BOUNDS
     assert torch.isfinite(run.out[:20].float()).all()   # request 0 unaffected
-    del snap
+    torch.cuda.synchronize()
+    assert bool((big[:, n_pages:].view(torch.int16) == -1).all())   # spare pages untouched
     run.close()
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    # Failure detection without a GPU fault: the test hook makes the leading CTA of each pair
+    # withhold its first key-tile arrival (no copy is issued for it), so the QK issuer's wait
+    # on that slot can never complete; with a 50 ms limit every role of both CTAs gives up,
+    # the pair drains, frees its tensor memory and returns, and the status word reports the
+    # timeout. A later call with the hook off is checked against the oracle.
+    import parity as PT
+    from oracle import oracle as O
+    from paged_sliding_window_qkv_gb300.runner import device_to_bits
+    for fam, n in ((W.HD256, 512), (W.HD512, 256)):
+        fi = W.custom_family(fam, [n], [0], seed=31, pool_fill="normal")
+        run = FamilyRun(fi)
+        torch.cuda.synchronize()
+        assert pg.pg_device_status() == pg.PG_OK
+        try:
+            assert pg.pg_test_bounded_wait(1, 50_000_000) == pg.PG_OK
+            assert run.attn_status(q=run.q_raw) == pg.PG_OK
+            assert pg.pg_device_status() == pg.PG_ERR_DEVICE_TIMEOUT
+        finally:
+            assert pg.pg_test_bounded_wait(0) == pg.PG_OK
+        assert pg.pg_device_status() == pg.PG_OK
+        run.attn(q=run.q_raw)
+        torch.cuda.synchronize()
+        assert pg.pg_device_status() == pg.PG_OK
+        ref = PT.attn_reference(fi, fi.q_raw, device_to_bits(run.pool),
+                                rows=np.array([[t, h] for t in (0, n // 2, n - 1) for h in range(16)]))
+        got = PT.bf16_out(run)
+        rows = [(t, h) for t in (0, n // 2, n - 1) for h in range(16)]
+        PT.attn_gate(np.stack([got[t, h] for t, h in rows]), ref, f"{fam.name} after a timeout")
+        run.close()
+    assert pg.pg_test_bounded_wait(2, 50_000_000) == pg.PG_ERR_ARG
+    assert pg.pg_test_bounded_wait(1, 10) == pg.PG_ERR_ARG
 
 
 def test_ring_and_segment_plans_update_in_place_and_survive_a_failed_update():
