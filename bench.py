@@ -11,7 +11,12 @@ before the timed region; L2 is flushed (a 512 MiB write) between timed steps.
 
 value: effective attention TFLOP/s of the whole step, 4*D*Hq*(visible query-key
 pairs) summed over the step's attention calls / step time. Per-kernel throughput
-(prep and decode GB/s, prefill TFLOP/s) is reported under "kernels".
+(prep and decode GB/s, prefill TFLOP/s) is reported under "kernels", each as a fraction of
+the measured peaks (frac_measured: MEASURED_PEAKS.json's HBM copy rate and burst bf16 GEMM
+rate, since every call runs for milliseconds at most) and of the nominal ones the targets are
+stated against (frac_nominal: 8 TB/s HBM, 2.25 PFLOP/s dense bf16). Outside the timed step:
+the batched ragged prefill (8 requests of 128-2048 tokens, 4 layers of 8192 pages) and the
+decode step replayed as one CUDA graph.
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
 """
@@ -38,6 +43,10 @@ WORKLOAD = ("mixed serving step, one layer per family: 16384-token prefill (hd25
 L2_FLUSH_BYTES = 512 << 20
 
 
+NOMINAL_HBM_GBS = 8000.0       # HBM3e, nominal
+NOMINAL_BF16_TFLOPS = 2250.0   # dense bf16 tensor rate, nominal
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -45,6 +54,18 @@ def load_peaks():
         return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
                     bf16_sustained=d["bf16_tflops_sustained"], src="measured")
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+def rate_entry(ms, work, kind, peaks):
+    """Per-call throughput: kind "hbm" (work in bytes) or "tensor" (work in FLOP), as achieved
+    rate and as fractions of the measured burst peak and of the nominal peak."""
+    if kind == "hbm":
+        gbs = work / (ms * 1e-3) / 1e9
+        return {"ms": ms, "GB/s": gbs, "bytes": work, "frac_measured": gbs / peaks["hbm"],
+                "frac_nominal": gbs / NOMINAL_HBM_GBS}
+    tf = work / (ms * 1e-3) / 1e12
+    return {"ms": ms, "TFLOP/s": tf, "flops": work, "frac_measured": tf / peaks["bf16"],
+            "frac_nominal": tf / NOMINAL_BF16_TFLOPS}
 
 
 # ---------------------------------------------------------------------------- work model
@@ -295,22 +316,38 @@ def run_reference(args):
 
 
 def kernel_traffic(call_name):
-    """DRAM bytes per launch of a call from the committed ncu summary (profiles/traffic.md),
+    """DRAM bytes per launch of a call from the committed ncu summary (profiles/traffic.json),
     if that capture was taken on the current kernel source; otherwise None."""
-    p = os.path.join(ROOT, "profiles", "traffic.md")
+    p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    for line in open(p):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) < 4 or cells[0] != call_name:
-            continue
-        src = os.path.join(ROOT, "paged_sliding_window_qkv_gb300", "csrc", cells[1])
-        if not os.path.exists(src):
-            return None
-        if hashlib.sha256(open(src, "rb").read()).hexdigest() != cells[2]:
-            return None
-        return int(cells[3])
-    return None
+    ent = json.load(open(p)).get("calls", {}).get(call_name)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "paged_sliding_window_qkv_gb300", "csrc", ent["source"])
+    if not os.path.exists(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != ent["sha256"]:
+        return None
+    return int(ent["dram_bytes_per_launch"])
+
+
+def time_calls(calls, stream, flush, reps):
+    """Median CUDA-event time (ms) of each zero-argument call, L2 flushed before each rep."""
+    import torch
+    out = []
+    for c in calls:
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            c()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        out.append(statistics.median(ts))
+    return out
 
 
 def run_ours(args):
@@ -325,7 +362,10 @@ def run_ours(args):
     from paged_sliding_window_qkv_gb300.runner import FamilyRun
 
     peaks = load_peaks()
-    stream = torch.cuda.current_stream()
+    # every call runs on one non-default stream (the plans are bound to it, and the decode
+    # step's CUDA-graph capture needs a capturable stream); torch's work joins it too
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
     # each rank owns its own requests (weak scaling; no exchange step on this path)
     seed5, seed4 = rank_seeds(rank)
     wl5 = W.make_workload(5, seed=seed5)
@@ -388,35 +428,69 @@ def run_ours(args):
 
     kernels = {}
     for i, (name, fi) in enumerate(fams):
-        pb = prep_bytes(fi)
-        kernels[name + " prep"] = {"ms": avg[2 * i], "GB/s": pb / (avg[2 * i] * 1e-3) / 1e9,
-                                   "frac_hbm": pb / (avg[2 * i] * 1e-3) / 1e9 / peaks["hbm"],
-                                   "bytes": pb}
-        ent = {"ms": avg[2 * i + 1], "TFLOP/s": flops[i] / (avg[2 * i + 1] * 1e-3) / 1e12}
+        kernels[name + " prep"] = rate_entry(avg[2 * i], prep_bytes(fi), "hbm", peaks)
         if name.startswith("decode"):
-            db = decode_bytes(fi)
-            ent.update({"GB/s": db / (avg[2 * i + 1] * 1e-3) / 1e9,
-                        "frac_hbm": db / (avg[2 * i + 1] * 1e-3) / 1e9 / peaks["hbm"],
-                        "bytes": db})
+            ent = rate_entry(avg[2 * i + 1], decode_bytes(fi), "hbm", peaks)
+            ent["TFLOP/s"] = flops[i] / (avg[2 * i + 1] * 1e-3) / 1e12
         else:
-            ent["frac_bf16"] = ent["TFLOP/s"] / peaks["bf16_sustained"]
-            ent["flops"] = flops[i]
+            ent = rate_entry(avg[2 * i + 1], flops[i], "tensor", peaks)
         kernels[name + " attention"] = ent
 
-    # dominant kernel: the call with the largest share of the step
+    # dominant kernel: the call with the largest share of the step. Every call runs for
+    # milliseconds at most, so the burst bf16 peak applies.
     dom_i = int(np.argmax(avg))
     dom_name = list(kernels)[dom_i]
     dom = kernels[dom_name]
-    if "frac_bf16" in dom:
+    if "flops" in dom:
         roof = {"kernel": dom_name, "bound": "tensor", "achieved": dom["TFLOP/s"],
-                "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                "frac": dom["TFLOP/s"] / peaks["bf16_sustained"],
-                "peak_kind": f"bf16 sustained, {peaks['src']}"}
+                "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": dom["TFLOP/s"] / peaks["bf16"],
+                "frac_nominal": dom["TFLOP/s"] / NOMINAL_BF16_TFLOPS,
+                "peak_kind": f"bf16 burst, {peaks['src']}; frac_nominal against 2.25 PFLOP/s"}
     else:
         roof = {"kernel": dom_name, "bound": "hbm", "achieved": dom["GB/s"], "peak": peaks["hbm"],
                 "unit": "GB/s", "frac": dom["GB/s"] / peaks["hbm"],
-                "peak_kind": f"hbm copy, {peaks['src']}"}
+                "frac_nominal": dom["GB/s"] / NOMINAL_HBM_GBS,
+                "peak_kind": f"hbm copy, {peaks['src']}; frac_nominal against 8 TB/s"}
+    roof["share_of_step"] = float(avg[dom_i] / avg.sum())
     roof["traffic"] = kernel_traffic(dom_name)
+
+    # ---- the decode step replayed as one CUDA graph (prep + attention of both families) ----
+    dec = [r for name, r in runs if name.startswith("decode")]
+
+    def decode_step():
+        for r in dec:
+            pg.check(r.prep_status(), "decode prep")
+            pg.check(r.attn_status(), "decode attention")
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        decode_step()
+    torch.cuda.synchronize()
+    g_ms, e_ms = time_calls([graph.replay, decode_step], stream, flush, max(5, min(20, args.steps)))
+    kernels["decode step as one CUDA graph"] = {
+        "ms_graph": g_ms, "ms_eager": e_ms, "ms_eager_in_step": float(avg[4:8].sum()),
+        "GB/s_graph": (sum(decode_bytes(fi) + prep_bytes(fi) for n, fi in fams
+                           if n.startswith("decode")) / (g_ms * 1e-3) / 1e9)}
+    del graph
+
+    # ---- batched ragged prefill (8 requests x U[128, 2048] tokens, 4 layers x 8192 pages) ----
+    if not args.no_extra:
+        fi3 = W.make_workload(3, seed=1003 + 7919 * rank).families[0]
+        r3 = FamilyRun(fi3, stream=stream)
+        reps = max(5, min(20, args.steps))
+        for _ in range(3):
+            pg.check(r3.prep_status(), "cfg3 prep")
+            pg.check(r3.attn_status(), "cfg3 attention")
+        p_ms, a_ms = time_calls([lambda: pg.check(r3.prep_status(), "cfg3 prep"),
+                                 lambda: pg.check(r3.attn_status(), "cfg3 attention")],
+                                stream, flush, reps)
+        kernels["batched prefill hd256 prep (8 requests, 4x8192-page pool)"] = rate_entry(
+            p_ms, prep_bytes(fi3), "hbm", peaks)
+        kernels["batched prefill hd256 attention (8 requests, 4x8192-page pool)"] = rate_entry(
+            a_ms, attn_flops(fi3), "tensor", peaks)
+        r3.close()
+        del r3
+    assert pg.pg_device_status() == pg.PG_OK
 
     # ---- end to end through the public API with host buffers ----
     # Each call's inputs are copied in from pinned host memory on a copy stream and its output
@@ -429,6 +503,8 @@ def run_ours(args):
     inputs, outputs = [], []
     h2d = d2h = 0
     for _, r in runs:
+        # every step rebuilds the call's plan in place and uploads its metadata
+        h2d += int(r.plan.info().metadata_bytes)
         pairs = []
         for t in [r.q_raw, r.k_raw, r.v_raw]:
             if t is None:
@@ -457,6 +533,11 @@ def run_ours(args):
             landed[i] = ev
         for i in e2e_order:
             name, r = runs[i]
+            b = r.fi.batch
+            rc, _ = pg.pg_plan_paged_prefill(r.plan, b.num_req, b.qo_indptr, b.kv_page_indptr,
+                                             b.page_ids, b.last_page_len, b.start_pos, r.Hq, r.Hkv,
+                                             r.D, b.page_size, stream)
+            pg.check(rc, name + " plan")
             stream.wait_event(landed[i])
             pg.check(r.prep_status(), name + " prep")
             pg.check(r.attn_status(), name + " attention")
@@ -496,6 +577,8 @@ def run_ours(args):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded bf16 N(0,1), page ids shuffled)",
                 "config": {"workload": WORKLOAD, "tokens_prefill": 16384, "decode_requests": 64,
+                           "e2e": "pinned host inputs in, attention outputs out, and every call's "
+                                  "plan rebuilt in place and uploaded, inside the timed region",
                            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
                            "parallelism": f"replicas x{world} (independent requests per GPU)"},
                 "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
@@ -508,6 +591,211 @@ def run_ours(args):
     return 0
 
 
+
+# ---------------------------------------------------------------------------- next rows
+NEXT_CASES = ("merge", "cascade-decode-hd512", "ring-decode-hd256", "ring-prefill-hd256")
+
+
+def timed(fn, iters, flush):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return float(np.median([a.elapsed_time(b) for a, b in ev]))
+
+
+def randn_bf16(shape, gen):
+    return torch.randn(shape, generator=gen, device="cuda", dtype=torch.bfloat16)
+
+
+class Attn:
+    """One attention call on a plan over a pool, with its output and workspace."""
+
+    def __init__(self, plan, pool, q, D, window, lse=False):
+        self.plan, self.pool, self.q, self.D, self.window = plan, pool, q, D, window
+        self.desc = pg.pool_descriptor(pool)
+        self.out = torch.empty_like(q)
+        self.lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device="cuda") if lse else None
+        self.wsb = pg.pg_workspace_bytes(plan)
+        self.ws = torch.empty(self.wsb, dtype=torch.uint8, device="cuda") if self.wsb else None
+
+    def __call__(self):
+        if self.lse is None:
+            fn = pg.pg_attn_paged_prefill if self.D == 256 else pg.pg_attn_paged_prefill_hd512
+            rc = fn(self.plan, self.desc, 0, self.q, self.out, self.window, 1.0, self.ws, self.wsb)
+        else:
+            fn = pg.pg_attn_paged_prefill_lse if self.D == 256 else pg.pg_attn_paged_prefill_hd512_lse
+            rc = fn(self.plan, self.desc, 0, self.q, self.out, self.lse, self.window, 1.0, self.ws,
+                    self.wsb)
+        pg.check(rc, "attention")
+
+
+def table(lens, ps, first_page):
+    """Page table (indptr, ids, last_page_len) for runs of the given lengths on consecutive
+    page ids from first_page (the ids are permuted by the caller)."""
+    lens = np.asarray(lens, np.int64)
+    n = -(-lens // ps)
+    indptr = np.zeros(len(lens) + 1, np.int64)
+    indptr[1:] = np.cumsum(n)
+    ids = np.arange(first_page, first_page + indptr[-1], dtype=np.int64)
+    last = (lens - (n - 1) * ps).astype(np.int32)
+    return indptr, ids, last
+
+
+def case_merge(iters, flush, hbm):
+    gen = torch.Generator(device="cuda").manual_seed(1)
+    rows, D = 16384 * 16, 512
+    oa, ob = randn_bf16((rows, D), gen), randn_bf16((rows, D), gen)
+    la = torch.randn(rows, generator=gen, device="cuda") * 4
+    lb = torch.randn(rows, generator=gen, device="cuda") * 4
+    o = torch.empty_like(oa)
+    lo = torch.empty_like(la)
+    ms = timed(lambda: pg.check(pg.pg_merge_attn_states(oa, la, ob, lb, o, lo, rows, D), "merge"),
+               iters, flush)
+    nbytes = rows * (3 * D * 2 + 12)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"case": "merge", "rows": rows, "head_dim": D, "ms": ms, "bytes": nbytes,
+            "GB/s": gbs, "frac_hbm": gbs / hbm}
+
+
+def case_cascade(iters, flush, hbm):
+    rng = np.random.Generator(np.random.PCG64(11))
+    R, P, ps, hq, hkv, D = 64, 8192, 16, 16, 1, 512
+    own = rng.integers(1, 1025, R)
+    L = P + own
+    one = np.arange(R + 1, dtype=np.int64)
+    start = (L - 1).astype(np.int64)
+    # page ids: full copies, then the shared prefix, then the own runs; permuted over the pool
+    f_ip, f_ids, f_last = table(L, ps, 0)
+    n_pre = -(-P // ps)
+    p_ids = np.arange(f_ids.size, f_ids.size + n_pre)
+    s_ip, s_ids, s_last = table(own, ps, f_ids.size + n_pre)
+    total = int(s_ids[-1]) + 1
+    perm = rng.permutation(total).astype(np.int32)
+    gen = torch.Generator(device="cuda").manual_seed(2)
+    pool = randn_bf16((1, total, 2, hkv, ps, D), gen)
+    q = randn_bf16((R, hq, D), gen)
+
+    def plan(ip, ids, last, kv_start=None):
+        if kv_start is None:
+            rc, pl = pg.pg_plan_paged_prefill(None, R, one, ip, perm[ids], last, start, hq, hkv, D, ps)
+        else:
+            rc, pl = pg.pg_plan_paged_segment(None, R, one, ip, perm[ids], last, kv_start, start,
+                                              hq, hkv, D, ps)
+        pg.check(rc, "plan")
+        return pl
+
+    full = Attn(plan(f_ip, f_ids, f_last), pool, q, D, -1)
+    pre_ip = np.arange(R + 1, dtype=np.int64) * n_pre
+    pre = Attn(plan(pre_ip, np.tile(p_ids, R), np.full(R, P - (n_pre - 1) * ps, np.int32),
+                    np.zeros(R, np.int64)), pool, q, D, -1, lse=True)
+    suf = Attn(plan(s_ip, s_ids, s_last, np.full(R, P, np.int64)), pool, q, D, -1, lse=True)
+    out = torch.empty_like(q)
+    lse = torch.empty(R, hq, dtype=torch.float32, device="cuda")
+
+    def cascade():
+        pre()
+        suf()
+        pg.check(pg.pg_merge_attn_states(pre.out, pre.lse, suf.out, suf.lse, out, lse, R * hq, D),
+                 "merge")
+
+    t_full = timed(full, iters, flush)
+    t_cas = timed(cascade, iters, flush)
+    nbytes = int(L.sum()) * hkv * D * 2 * 2 + 2 * R * hq * D * 2
+    return {"case": "cascade-decode-hd512", "requests": R, "shared_prefix": P,
+            "own_tokens": "U[1,1024]", "single_pass_ms": t_full, "cascade_ms": t_cas,
+            "speedup": t_full / t_cas, "single_pass_bytes": nbytes,
+            "single_pass_GB/s": nbytes / (t_full * 1e-3) / 1e9,
+            "single_pass_frac_hbm": nbytes / (t_full * 1e-3) / 1e9 / hbm,
+            "cascade_effective_GB/s": nbytes / (t_cas * 1e-3) / 1e9}
+
+
+def ring_vs_linear(name, starts, qo_lens, window, hq, hkv, D, ps, iters, flush, work, unit):
+    R = len(starts)
+    qo = np.zeros(R + 1, np.int64)
+    qo[1:] = np.cumsum(qo_lens)
+    starts = np.asarray(starts, np.int64)
+    ring_pages = -(-(window + np.asarray(qo_lens)) // ps) + 1
+    r_ip = np.zeros(R + 1, np.int64)
+    r_ip[1:] = np.cumsum(ring_pages)
+    L = starts + np.asarray(qo_lens)
+    l_ip, l_ids, l_last = table(L, ps, int(r_ip[-1]))
+    total = int(l_ids[-1]) + 1
+    rng = np.random.Generator(np.random.PCG64(13))
+    perm = rng.permutation(total).astype(np.int32)
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    pool = randn_bf16((1, total, 2, hkv, ps, D), gen)
+    q = randn_bf16((int(qo[-1]), hq, D), gen)
+    rc, ring = pg.pg_plan_paged_prefill_ring(None, R, qo, r_ip, perm[:r_ip[-1]], starts, hq, hkv,
+                                             D, ps, window)
+    pg.check(rc, "ring plan")
+    rc, lin = pg.pg_plan_paged_prefill(None, R, qo, l_ip, perm[l_ids], l_last, starts, hq, hkv, D, ps)
+    pg.check(rc, "linear plan")
+    t_ring = timed(Attn(ring, pool, q, D, window), iters, flush)
+    t_lin = timed(Attn(lin, pool, q, D, window), iters, flush)
+    res = {"case": name, "requests": R, "window_left": window, "ring_ms": t_ring,
+           "linear_ms": t_lin, "work": work, "unit": unit,
+           "ring_rate": work / (t_ring * 1e-3) / (1e9 if unit == "B" else 1e12),
+           "linear_rate": work / (t_lin * 1e-3) / (1e9 if unit == "B" else 1e12)}
+    return res
+
+
+def run_next_rows(args):
+    """Calls beyond the single step, one JSON line per case (CUDA events, median of --steps calls
+    after 3 warm-up calls, L2 flushed by a 512 MiB write before each call). Attention here only
+    reads the pool, so the pools hold N(0,1) bf16 written directly and the queries are N(0,1)
+    bf16. Cases:
+
+    * merge: merging two attention states of 16384 tokens x 16 heads at head_dim 512
+      (pg_merge_attn_states); bytes = rows x (3 x 512 x 2 + 12).
+    * cascade-decode-hd512: a decode step of 64 requests sharing an 8192-token prefix and holding
+      U[1, 1024] tokens of their own, full causal: the single pass over each request's own copy of
+      all its keys, against the cascade (the prefix as one key segment listed for every request,
+      the own keys as another, and the merge). Bytes are the single pass's K/V reads.
+    * ring-decode-hd256: a decode step of 64 requests at positions U[4096, 32768) holding a ring
+      of ceil((window + 1) / 16) + 1 pages, window_left 1023, against the same window on linear
+      pages; bytes = visible keys x 8 heads x 256 x 2 x 2.
+    * ring-prefill-hd256: a 4096-token chunk at position 65536 of one request on a ring of
+      ceil((window + 4096) / 16) + 1 pages, window_left 1023, against linear pages;
+      FLOP = 4 x 256 x 16 x visible pairs.
+    """
+    # the case helpers above use these two modules as globals
+    global pg, torch
+    import torch
+    from paged_sliding_window_qkv_gb300 import pg
+    peaks = load_peaks()
+    hbm, bf16 = peaks["hbm"], peaks["bf16"]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    iters = max(5, args.steps)
+    for c in NEXT_CASES:
+        if c == "merge":
+            res = case_merge(iters, flush, hbm)
+        elif c == "cascade-decode-hd512":
+            res = case_cascade(iters, flush, hbm)
+        elif c == "ring-decode-hd256":
+            rng = np.random.Generator(np.random.PCG64(17))
+            starts = rng.integers(4096, 32768, 64)
+            work = 64 * 1024 * 8 * 256 * 2 * 2
+            res = ring_vs_linear(c, starts, [1] * 64, 1023, 16, 8, 256, 16, iters, flush,
+                                 work, "B")
+            res["frac_hbm_ring"] = res["ring_rate"] / hbm
+        else:
+            pairs = sum(min(p + 1, 1024) for p in range(65536, 65536 + 4096))
+            res = ring_vs_linear(c, [65536], [4096], 1023, 16, 8, 256, 16, iters, flush,
+                                 4.0 * 256 * 16 * pairs, "FLOP")
+            res["frac_bf16_ring"] = res["ring_rate"] / bf16
+        res["peaks"] = peaks["src"]
+        print(json.dumps(res), flush=True)
+    return 0 if pg.pg_device_status() == pg.PG_OK else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,7 +804,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the batched-prefill measurement outside the timed step")
+    ap.add_argument("--next-rows", action="store_true",
+                    help="time the calls beyond the step (merge, cascade, ring) and exit")
     args = ap.parse_args()
+    if args.next_rows:
+        return run_next_rows(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

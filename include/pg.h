@@ -187,6 +187,7 @@ typedef struct {
   int32_t num_work;         /* prefill work items (request, query tile)                */
   const int32_t* d_page_ids;/* device copy of page_ids (for diagnostics)              */
   pg_stream_t stream;
+  int64_t metadata_bytes;   /* bytes of device metadata each build or update uploads  */
 } pg_plan_info_t;
 
 /* Copy the plan's recorded geometry and bounds into *info. */

@@ -567,6 +567,7 @@ int pg_plan_info(const pg_plan_t p, pg_plan_info_t* info) {
   info->num_work = p->num_work;
   info->d_page_ids = p->dev + p->o_pages;
   info->stream = reinterpret_cast<pg_stream_t>(p->stream);
+  info->metadata_bytes = (int64_t)p->dev_elems * (int64_t)sizeof(int32_t);
   return PG_OK;
 }
 

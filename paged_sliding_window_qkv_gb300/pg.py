@@ -67,7 +67,7 @@ class pg_plan_info_t(C.Structure):
         "num_req", "num_tokens", "num_qo_heads", "num_kv_heads", "head_dim", "page_size",
         "max_page_id", "max_last_page_len", "max_qo_len", "max_kv_len", "max_pos_end",
         "cta_tile_q", "decode", "kv_chunk", "max_chunks", "num_work")] + [
-        ("d_page_ids", C.c_void_p), ("stream", C.c_void_p)]
+        ("d_page_ids", C.c_void_p), ("stream", C.c_void_p), ("metadata_bytes", C.c_int64)]
 
 
 _P = C.c_void_p

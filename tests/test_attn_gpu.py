@@ -138,9 +138,11 @@ def test_end_to_end_prep_then_attention(cfg):
         run.close()
 
 
-def test_full_size_config5_sampled_rows():
-    # the long 16384-token prefill of both families, in the launch the benchmark times;
-    # the oracle evaluates a sample of rows one by one
+def test_full_size_config5_rows():
+    # The long 16384-token prefill of both families in the launch the benchmark times, after
+    # the prep it times. The oracle (fp64) evaluates every row of two seeded heads plus every
+    # head of 512 seeded tokens (first, last and window-edge tokens among them), on the pool
+    # and queries the oracle's own prep would produce.
     wl = W.make_workload(5)
     rng = np.random.Generator(np.random.PCG64(55))
     for fi in wl.families:
@@ -148,9 +150,14 @@ def test_full_size_config5_sampled_rows():
         run.prep()
         run.attn()
         gpu = parity.bf16_out(run)
-        T = fi.batch.num_tokens
-        toks = np.concatenate([[0, 1, T - 1, T - 2, 1023, 1024], rng.integers(0, T, 58)])
-        rows = np.stack([toks, rng.integers(0, 16, len(toks))], axis=1)
+        T, Hq = fi.batch.num_tokens, fi.family.num_qo_heads
+        heads = rng.choice(Hq, 2, replace=False)
+        toks = np.unique(np.concatenate([[0, 1, 63, 64, 127, 128, 1023, 1024, 1025, T - 2, T - 1],
+                                         rng.choice(T, 512 - 11, replace=False)]))
+        rows = np.concatenate([
+            np.stack(np.meshgrid(np.arange(T), heads, indexing="ij"), axis=-1).reshape(-1, 2),
+            np.stack(np.meshgrid(toks, np.arange(Hq), indexing="ij"), axis=-1).reshape(-1, 2)])
+        rows = np.unique(rows, axis=0)
         qo, ko, vo, offs = parity.prep_reference(fi)
         pool = fi.make_pool()
         D = fi.family.head_dim
@@ -158,7 +165,8 @@ def test_full_size_config5_sampled_rows():
         flat[(offs[:, 0] // D).ravel()] = O.f64_to_bf16(ko).reshape(-1, D)
         flat[(offs[:, 1] // D).ravel()] = O.f64_to_bf16(vo).reshape(-1, D)
         ref = parity.attn_reference(fi, O.f64_to_bf16(qo), pool, rows=rows)
-        parity.attn_gate(gpu[rows[:, 0], rows[:, 1]], ref, f"cfg5 {fi.family.name} sampled")
+        parity.attn_gate(gpu[rows[:, 0], rows[:, 1]], ref,
+                         f"cfg5 {fi.family.name}: {len(rows)} rows")
         run.close()
 
 

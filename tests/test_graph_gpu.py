@@ -1,14 +1,17 @@
 """The decode step of both families captured in one CUDA graph.
 
 The pages leave the decode form's launch shape open ("measurement-gated"); a serving loop
-replays the whole step (prep + attention of both families, six kernels) as one graph. The
-entry points make no allocation, synchronisation or host read on the stream once each kernel
-has been launched once, so the step can be captured; the replay must reproduce the eager
-outputs bit for bit.
+replays the whole step (prep + attention of both families) as one graph. The entry points make
+no allocation, synchronisation or host read on the stream once each kernel has been launched
+once, so the step can be captured. The replay is gated against the oracle (prep: q_out and the
+pool rows within one bf16 ulp, every other pool row byte-exact; attention: the oracle's
+attention over the replayed pool and q_out) and must also reproduce the eager step bit for bit.
 """
 import numpy as np
 import pytest
 import torch
+
+import parity as PT
 
 from paged_sliding_window_qkv_gb300 import pg
 from paged_sliding_window_qkv_gb300 import workloads as W
@@ -44,6 +47,10 @@ def test_decode_step_replays_as_one_graph():
         s.synchronize()
     assert launched == 6        # two preps, two split-KV attentions, two merges
     assert pg.pg_device_status() == pg.PG_OK
+    for r, fi in zip(runs, wl.families):
+        PT.check_prep(r, fi, initial_pool_bits=fi.make_pool())
+        ref = PT.attn_reference(fi, device_to_bits(r.q_out), device_to_bits(r.pool))
+        PT.attn_gate(PT.bf16_out(r), ref, f"graph replay {fi.family.name}")
     for r, o, p in zip(runs, eager_out, eager_pool):
         assert np.array_equal(device_to_bits(r.out), o)
         assert np.array_equal(device_to_bits(r.pool), p)

@@ -3,9 +3,10 @@
 pg_attn_paged_decode_noalloc serves callers that may not allocate device memory at call
 time (for example under an allocator that forbids cudaMalloc once serving has started);
 it keeps its split-KV partials in a static scratch buffer inside the library. These
-tests compare it with the workspace entry points on the same decode plans, twice in a
-row with different windows so the second call runs over the first call's leftovers, and
-check its size limit. This file is named to be collected last."""
+tests compare it with the fp64 oracle and with the workspace entry points on the same
+decode plans, twice in a row with different windows so the second call runs over the
+first call's leftovers, and check its size limit. This file is named to be collected
+last."""
 import numpy as np
 import pytest
 import torch
@@ -41,6 +42,8 @@ def test_noalloc_decode_matches_workspace_entry_on_two_calls(fam):
         rc = pg.pg_attn_paged_decode_noalloc(run.plan, run.pool_desc, fi.layer, run.q_raw, got,
                                              w, fi.sm_scale)
         assert rc == pg.PG_OK, pg.pg_status_string(rc)
+        oracle = parity.attn_reference(fi, fi.q_raw, device_to_bits(run.pool), window_left=w)
+        parity.attn_gate(_bits64(got), oracle, f"{fam.name} no-alloc decode vs oracle, window {w}")
         parity.attn_gate(_bits64(got), ref, f"{fam.name} no-alloc decode, window {w}")
     assert pg.pg_device_status() == pg.PG_OK
     run.close()
