@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libpg.so")
-SOURCES = ["pg_host.cpp", "pg_kv.cpp", "prep.cu", "attn_split.cu", "attn_tc.cu", "cascade.cu"]
+SOURCES = ["pg_host.cpp", "pg_kv.cpp", "prep.cu", "attn_split.cu", "attn_decode.cu", "attn_tc.cu", "cascade.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

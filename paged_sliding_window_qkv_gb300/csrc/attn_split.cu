@@ -482,8 +482,15 @@ cudaError_t launch_attn_prefill(const AttnArgs& a, int32_t head_dim, cudaStream_
                          : launch_split<Pre512>(a, grid, stream);
 }
 
-cudaError_t launch_attn_decode(const AttnArgs& a, int32_t head_dim, cudaStream_t stream) {
-  if (a.plan.num_req == 0) return cudaSuccess;
+cudaError_t launch_attn_decode(const AttnArgs& args, int32_t head_dim, cudaStream_t stream) {
+  if (args.plan.num_req == 0) return cudaSuccess;
+  if (attn_decode_stream_supported(head_dim, args.group, args.pool.page_size))
+    return launch_attn_decode_stream(args, head_dim, stream);
+  // other page sizes: fixed key chunks per (request, KV head), partials in the workspace
+  AttnArgs a = args;
+  const size_t rows = (size_t)a.plan.num_req * a.num_qo_heads * a.max_chunks;
+  a.ws_o = reinterpret_cast<float*>(a.ws_raw);
+  a.ws_ml = a.ws_o + rows * (size_t)head_dim;
   dim3 grid(a.plan.num_req, a.pool.num_kv_heads, a.max_chunks);
   cudaError_t e = head_dim == 256 ? launch_split<Dec256>(a, grid, stream)
                                   : launch_split<Dec512>(a, grid, stream);
@@ -521,9 +528,7 @@ cudaError_t launch_attn_decode_static(AttnArgs a, int32_t head_dim, cudaStream_t
     }
     base = g_decode_scratch_addr[dev];
   }
-  const size_t rows = (size_t)a.plan.num_req * a.num_qo_heads * a.max_chunks;
-  a.ws_o = reinterpret_cast<float*>(base);
-  a.ws_ml = a.ws_o + rows * (size_t)head_dim;
+  a.ws_raw = base;
   return launch_attn_decode(a, head_dim, stream);
 }
 

@@ -188,6 +188,12 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   // Tiling derived from the geometry; attention re-derives it from the kernel itself.
   const int32_t cta = plan_cta_tile_q(D, group, ps);
   const int32_t chunk = plan_kv_chunk(D);
+  {
+    // the chunked decode kernel holds a request's key chunks in its grid's z dimension
+    const int64_t seen = ring ? std::min<int64_t>(max_kv, (int64_t)ring_window + 1) : max_seen;
+    if (all_one && !attn_decode_stream_supported(D, group, ps) && (seen + chunk - 1) / chunk > 65535)
+      return PG_ERR_I32_OVERFLOW;
+  }
   int64_t nwork = 0;
   std::vector<int32_t> wreq, wtok, ptab;
   if (cta > 0) {
@@ -394,6 +400,9 @@ int prep_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
 
 size_t workspace_bytes(const pg_plan* p) {
   if (!p || !p->decode || p->num_req == 0) return 0;
+  const int32_t group = p->num_qo_heads / p->num_kv_heads;
+  if (attn_decode_stream_supported(p->head_dim, group, p->page_size))
+    return attn_decode_stream_ws_bytes(p->num_req, group, p->head_dim);
   const size_t rows = (size_t)p->num_req * p->num_qo_heads * p->max_chunks;
   return rows * (size_t)p->head_dim * sizeof(float) + rows * 2 * sizeof(float);
 }
@@ -413,8 +422,13 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
   // ring addressing holds only the window the plan was built for
   if (plan->ring && (window_left < 0 || window_left > plan->ring_window)) return PG_ERR_WINDOW;
   if (!std::isfinite(sm_scale)) return PG_ERR_NONFINITE;
-  if (!plan->decode && attn_tc_supported(D, group, plan->page_size) &&
-      (int64_t)pool->num_pages * 2 * pool->num_kv_heads * pool->page_size > INT32_MAX)
+  const bool tma_rows = plan->decode ? attn_decode_stream_supported(D, group, plan->page_size)
+                                     : attn_tc_supported(D, group, plan->page_size);
+  // the chunked decode kernel's grid holds the key chunks of a request in its z dimension
+  if (plan->decode && !attn_decode_stream_supported(D, group, plan->page_size) &&
+      plan->max_chunks > 65535)
+    return PG_ERR_I32_OVERFLOW;
+  if (tma_rows && (int64_t)pool->num_pages * 2 * pool->num_kv_heads * pool->page_size > INT32_MAX)
     return PG_ERR_I32_OVERFLOW;  // tensor-map row coordinates are int32
   if (plan->num_tokens == 0) return PG_OK;
   if (!q || !out) return PG_ERR_ARG;
@@ -444,14 +458,12 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
   a.status = st;
   wait_settings(&a.wait_ns, &a.test_withhold);
   cudaError_t e;
+  a.ws_raw = ws;
+  a.ws_o = nullptr;
+  a.ws_ml = nullptr;
   if (plan->decode) {
-    const size_t rows = (size_t)plan->num_req * plan->num_qo_heads * plan->max_chunks;
-    a.ws_o = reinterpret_cast<float*>(ws);
-    a.ws_ml = a.ws_o + rows * (size_t)D;
     e = launch_attn_decode(a, D, stream);
   } else {
-    a.ws_o = nullptr;
-    a.ws_ml = nullptr;
     e = launch_attn_prefill(a, D, stream);
   }
   return e == cudaSuccess ? PG_OK : PG_ERR_CUDA;
@@ -684,6 +696,11 @@ int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, in
   if (window_left < -1) return PG_ERR_WINDOW;
   if (plan->ring && (window_left < 0 || window_left > plan->ring_window)) return PG_ERR_WINDOW;
   if (!std::isfinite(sm_scale)) return PG_ERR_NONFINITE;
+  if (attn_decode_stream_supported(D, group, plan->page_size) &&
+      (int64_t)pool->num_pages * 2 * pool->num_kv_heads * pool->page_size > INT32_MAX)
+    return PG_ERR_I32_OVERFLOW;  // tensor-map row coordinates are int32
+  if (!attn_decode_stream_supported(D, group, plan->page_size) && plan->max_chunks > 65535)
+    return PG_ERR_I32_OVERFLOW;  // the chunked kernel's grid z dimension
   if (plan->num_tokens == 0) return PG_OK;
   if (!q || !out) return PG_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return PG_ERR_ALIGN;
@@ -696,6 +713,7 @@ int pg_attn_paged_decode_noalloc(const pg_plan_t plan, const pg_pool_t* pool, in
   a.q = reinterpret_cast<const __nv_bfloat16*>(q);
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
   a.lse = nullptr;
+  a.ws_raw = nullptr;
   a.ws_o = nullptr;
   a.ws_ml = nullptr;
   a.sm_scale_log2 = sm_scale * 1.4426950408889634f;

@@ -79,8 +79,9 @@ struct AttnArgs {
   const __nv_bfloat16* q;
   __nv_bfloat16* out;
   float* lse;     // optional [T][Hq] natural-log normaliser of each row (null: not written)
-  float* ws_o;    // decode form: partial outputs [R][Hq][max_chunks][D]
-  float* ws_ml;   // decode form: [R][Hq][max_chunks][2] (running max in log2 units, sum)
+  void* ws_raw;   // decode form: the caller's workspace (pg_workspace_bytes), 16-byte aligned
+  float* ws_o;    // chunked decode form: partial outputs [R][Hq][max_chunks][D]
+  float* ws_ml;   // chunked decode form: [R][Hq][max_chunks][2] (running max in log2 units, sum)
   float sm_scale_log2;  // sm_scale * log2(e)
   int32_t window_left;
   int32_t num_qo_heads;
@@ -121,6 +122,12 @@ cudaError_t launch_attn_prefill_tc(const AttnArgs& a, int32_t head_dim, cudaStre
 int32_t attn_kernel_kv_chunk(int32_t head_dim);
 cudaError_t launch_attn_prefill(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);
 cudaError_t launch_attn_decode(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);
+// Decode as one balanced stream over the step's visible keys (TMA-fed, persistent): the
+// geometry it handles (head_dim 256/512, group <= 16, power-of-two page size), the workspace
+// it needs, and its launch (decode kernel + merge of the segments cut between CTAs).
+bool attn_decode_stream_supported(int32_t head_dim, int32_t group, int32_t page_size);
+size_t attn_decode_stream_ws_bytes(int32_t num_req, int32_t group, int32_t head_dim);
+cudaError_t launch_attn_decode_stream(const AttnArgs& a, int32_t head_dim, cudaStream_t stream);
 
 // Decode attention with its partials in the library's static scratch (no allocation).
 // The caller has already checked the plan's workspace size against that scratch.

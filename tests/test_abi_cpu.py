@@ -67,6 +67,16 @@ def test_more_plan_rejects(name):
     assert plan is None
 
 
+def test_decode_plan_past_the_chunked_grid_is_rejected():
+    # head_dim 512 decode runs in 512-key chunks, one grid z index each: a request that sees more
+    # than 65535 chunks (33,553,921 keys and up) cannot be launched and is refused at plan time
+    ps, kv = 12, 65535 * 512 + 1
+    npages = -(-kv // ps)
+    rc, plan = pg.pg_plan_paged_prefill(None, 1, [0, 1], [0, npages], np.arange(npages, dtype=np.int32),
+                                        [kv - (npages - 1) * ps], [kv - 1], 16, 1, 512, ps, stream=0)
+    assert rc == pg.PG_ERR_I32_OVERFLOW and plan is None
+
+
 def test_zero_kv_heads_wins_over_other_faults():
     # the head relation is settled first, before anything could divide by it
     a = rejects.plan_case("zero_kv_heads")

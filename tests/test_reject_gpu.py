@@ -207,7 +207,8 @@ def test_device_second_layer_flags_and_skips_bad_page_ids():
                      device="cuda").view(torch.bfloat16)
     run.pool = big[:, :n_pages]
     assert run.pool.is_contiguous()
-    run.pool_desc = pg.pool_descriptor(run.pool)
+    # one layer: its stride is the dense one, whatever the allocation behind it holds
+    run.pool_desc = pg.pool_descriptor(run.pool, stride_layer=run.pool.stride(1) * n_pages)
     assert run.pool_desc.num_pages == n_pages
     info = run.plan.info()
     # corrupt the device copy of the first page id of request 1 (host bounds stay valid)

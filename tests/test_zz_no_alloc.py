@@ -50,12 +50,13 @@ def test_noalloc_decode_matches_workspace_entry_on_two_calls(fam):
 
 
 def test_noalloc_rejects_oversized_and_prefill_plans():
-    # a decode plan whose partials need more than the static scratch holds
+    # a decode plan whose partials need more than the static scratch holds: at page size 12 the
+    # decode runs in fixed key chunks with one partial per (request, head, chunk)
     R, kv = 64, 16384
     rng = np.random.Generator(np.random.PCG64(79))
-    b = W.make_batch(rng, np.ones(R, np.int64), np.full(R, kv - 1), 16)
+    b = W.make_batch(rng, np.ones(R, np.int64), np.full(R, kv - 1), 12)
     rc, plan = pg.pg_plan_paged_prefill(None, R, b.qo_indptr, b.kv_page_indptr, b.page_ids,
-                                        b.last_page_len, b.start_pos, 16, 1, 512, 16)
+                                        b.last_page_len, b.start_pos, 16, 1, 512, 12)
     assert rc == pg.PG_OK
     assert pg.pg_workspace_bytes(plan) > pg.PG_NOALLOC_SCRATCH_BYTES
     small = torch.zeros(1, 4, 2, 1, 16, 512, dtype=torch.bfloat16, device="cuda")
