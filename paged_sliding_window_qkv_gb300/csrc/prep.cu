@@ -7,13 +7,15 @@
 // Q rows, K rows and V rows are contiguous runs) and its rotary row into a ring of
 // shared-memory stages with bulk asynchronous copies (cp.async.bulk, completion counted in
 // bytes on the stage's mbarrier), several tokens ahead, so every SM keeps hundreds of KB of
-// loads in flight without holding them in registers. Eight consumer warps each own whole
-// head rows of the staged token: a lane reads 16-byte vectors from shared memory (a 256-wide
-// row is one conflict-free 512-byte read per warp), the RMS reduction is a warp shuffle, each
-// lane holds both elements of its rotary pairs, and every
-// result row is one coalesced 512-byte (or 1 KB) store: q_out rows, or K/V rows at the
-// token's paged slot (slot = position, wrapped over the request's pages for a ring plan, or
-// counted from the segment's first position for a key-segment plan). The producer also resolves each token's request, position and page
+// loads in flight without holding them in registers. Eight consumer warps take the staged
+// token's head rows kind by kind, D / 16 lanes per row (two rows per warp at head_dim 256, one
+// at 512): a lane reads two 16-byte vectors from shared memory (its elements [8j, 8j + 8) and
+// their rotary partners D/2 further), the RMS reduction is a shuffle over the row's lanes, and
+// the normalisation, weight and rotation run on packed fp32 pairs, so the consumers stay
+// below the issue rate HBM allows. Every result row is written by coalesced 16-byte stores:
+// q_out rows, or K/V rows at the token's paged slot (slot = position, wrapped over the
+// request's pages for a ring plan, or counted from the segment's first position for a
+// key-segment plan). The producer also resolves each token's request, position and page
 // (32 tokens at a time, one per lane) and passes them to the consumers in the stage header.
 //
 // Waits are bounded (two seconds of %globaltimer); a wait that runs out sets the device
@@ -32,31 +34,6 @@ namespace {
 constexpr int kPrepConsumerWarps = 8;
 constexpr int kPrepThreads = (kPrepConsumerWarps + 1) * 32;  // + producer warp
 constexpr uint64_t kPrepWaitNs = 2000000000ull;
-
-__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ uint4 pack8(const float* f) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-    w[i] = *reinterpret_cast<uint32_t*>(&h);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -142,87 +119,68 @@ __device__ __forceinline__ bool token_meta(const PrepArgs& a, int32_t t, TokMeta
   return true;
 }
 
-// Normalise (and for Q/K rows weight and rotate) one staged row and store it. Each rotary pair
-// (i, i + D/2) sits in one lane, so the rotation needs no shuffle:
-//   D = 256: lane l holds elements [4l, 4l + 4) and [128 + 4l, 128 + 4l + 4);
-//   D = 512: lane l holds [8l, 8l + 8) and [256 + 8l, 256 + 8l + 8).
-// kind: 0 = Q, 1 = K, 2 = V (weightless, not rotated). For D = 512 a K row also writes its V
-// row: the weightless norm of the same raw row with the same inverse RMS.
-template <int D>
-__device__ __forceinline__ void prep_row(const PrepArgs& a, const unsigned char* row_smem, int kind,
-                                         int lane, const float* c, const float* s,
-                                         const float* w_lo, const float* w_hi,
-                                         __nv_bfloat16* dst, __nv_bfloat16* vdst) {
-  if constexpr (D == 256) {
-    // lane l: elements [4l, 4l + 4) and their rotary partners [128 + 4l, 128 + 4l + 4)
-    float xa[4], xb[4];
-    {
-      const uint2 va = *reinterpret_cast<const uint2*>(row_smem + lane * 8);
-      const uint2 vb = *reinterpret_cast<const uint2*>(row_smem + 256 + lane * 8);
-      xa[0] = __uint_as_float(va.x << 16); xa[1] = __uint_as_float(va.x & 0xFFFF0000u);
-      xa[2] = __uint_as_float(va.y << 16); xa[3] = __uint_as_float(va.y & 0xFFFF0000u);
-      xb[0] = __uint_as_float(vb.x << 16); xb[1] = __uint_as_float(vb.x & 0xFFFF0000u);
-      xb[2] = __uint_as_float(vb.y << 16); xb[3] = __uint_as_float(vb.y & 0xFFFF0000u);
-    }
-    float ss = 0.f;
+// One staged row, normalised (and for Q/K rows weighted and rotated), stored as bf16. A row is
+// handled by LPR = D / 16 lanes (a half warp at D = 256, a warp at D = 512); lane j of the row
+// holds its elements [8j, 8j + 8) and their rotary partners [D/2 + 8j, D/2 + 8j + 8), so every
+// rotary pair sits in one lane, and the arithmetic runs on packed fp32 pairs (f32x2), one bf16
+// round-to-nearest-even at the store.
+struct RowIn {
+  float2 a[4], b[4];  // elements [8j, 8j + 8) and [D/2 + 8j, D/2 + 8j + 8), in fp32 pairs
+};
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
+  __nv_bfloat162 h = __float22bfloat162_rn(v);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Loads lane j's 16 elements of a staged row and returns its inverse RMS (the sum of squares is
+// reduced over the LPR lanes of the row).
+template <int LPR>
+__device__ __forceinline__ float load_row(const unsigned char* row_smem, int j, int D2, float inv_d,
+                                          float eps, RowIn* x) {
+  const uint4 va = *reinterpret_cast<const uint4*>(row_smem + 16 * j);
+  const uint4 vb = *reinterpret_cast<const uint4*>(row_smem + D2 + 16 * j);
+  x->a[0] = bf2_to_f2(va.x); x->a[1] = bf2_to_f2(va.y); x->a[2] = bf2_to_f2(va.z); x->a[3] = bf2_to_f2(va.w);
+  x->b[0] = bf2_to_f2(vb.x); x->b[1] = bf2_to_f2(vb.y); x->b[2] = bf2_to_f2(vb.z); x->b[3] = bf2_to_f2(vb.w);
+  float2 ss = __fmul2_rn(x->a[0], x->a[0]);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) ss = fmaf(xa[e], xa[e], fmaf(xb[e], xb[e], ss));
-    ss = warp_sum(ss);
-    const float inv = 1.0f / sqrtf(ss * (1.0f / 256.0f) + a.eps);
-    float ya[4], yb[4];
-    if (kind == 2) {
+  for (int k = 1; k < 4; ++k) ss = __ffma2_rn(x->a[k], x->a[k], ss);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        ya[e] = xa[e] * inv;
-        yb[e] = xb[e] * inv;
-      }
-    } else {
+  for (int k = 0; k < 4; ++k) ss = __ffma2_rn(x->b[k], x->b[k], ss);
+  float t = ss.x + ss.y;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float ua = xa[e] * inv * w_lo[e];
-        const float ub = xb[e] * inv * w_hi[e];
-        ya[e] = ua * c[e] - ub * s[e];
-        yb[e] = ub * c[e] + ua * s[e];
-      }
-    }
-    uint2 oa, ob;
-    {
-      __nv_bfloat162 h0 = __floats2bfloat162_rn(ya[0], ya[1]), h1 = __floats2bfloat162_rn(ya[2], ya[3]);
-      __nv_bfloat162 h2 = __floats2bfloat162_rn(yb[0], yb[1]), h3 = __floats2bfloat162_rn(yb[2], yb[3]);
-      oa = make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
-      ob = make_uint2(*reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
-    }
-    *reinterpret_cast<uint2*>(dst + lane * 4) = oa;
-    *reinterpret_cast<uint2*>(dst + 128 + lane * 4) = ob;
-  } else {
-    float xa[8], xb[8];
-    unpack8(*reinterpret_cast<const uint4*>(row_smem + lane * 16), xa);
-    unpack8(*reinterpret_cast<const uint4*>(row_smem + 512 + lane * 16), xb);
-    float ss = 0.f;
+  for (int o = LPR / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return rsqrtf(t * inv_d + eps);
+}
+// y = x * inv (weightless, never rotated)
+__device__ __forceinline__ void store_plain(const RowIn& x, float inv, __nv_bfloat16* dst, int j,
+                                            int D2) {
+  const float2 iv = make_float2(inv, inv);
+  uint4 oa, ob;
+  oa.x = f2_to_bf2(__fmul2_rn(x.a[0], iv)); oa.y = f2_to_bf2(__fmul2_rn(x.a[1], iv));
+  oa.z = f2_to_bf2(__fmul2_rn(x.a[2], iv)); oa.w = f2_to_bf2(__fmul2_rn(x.a[3], iv));
+  ob.x = f2_to_bf2(__fmul2_rn(x.b[0], iv)); ob.y = f2_to_bf2(__fmul2_rn(x.b[1], iv));
+  ob.z = f2_to_bf2(__fmul2_rn(x.b[2], iv)); ob.w = f2_to_bf2(__fmul2_rn(x.b[3], iv));
+  *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(dst) + 16 * j) = oa;
+  *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(dst) + D2 + 16 * j) = ob;
+}
+// y = rope(x * inv * w): ya = inv (a wa c - b wb s), yb = inv (b wb c + a wa s); ns = -s
+__device__ __forceinline__ void store_rotated(const RowIn& x, float inv, const float2* wa,
+                                              const float2* wb, const float2* c, const float2* s,
+                                              const float2* ns, __nv_bfloat16* dst, int j, int D2) {
+  const float2 iv = make_float2(inv, inv);
+  uint32_t ya[4], yb[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(xa[e], xa[e], fmaf(xb[e], xb[e], ss));
-    ss = warp_sum(ss);
-    const float inv = 1.0f / sqrtf(ss * (1.0f / 512.0f) + a.eps);
-    float ya[8], yb[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float ua = xa[e] * inv * w_lo[e];
-      const float ub = xb[e] * inv * w_hi[e];
-      ya[e] = ua * c[e] - ub * s[e];
-      yb[e] = ub * c[e] + ua * s[e];
-    }
-    *reinterpret_cast<uint4*>(dst + lane * 8) = pack8(ya);
-    *reinterpret_cast<uint4*>(dst + 256 + lane * 8) = pack8(yb);
-    if (kind == 1) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ya[e] = xa[e] * inv;
-        yb[e] = xb[e] * inv;
-      }
-      *reinterpret_cast<uint4*>(vdst + lane * 8) = pack8(ya);
-      *reinterpret_cast<uint4*>(vdst + 256 + lane * 8) = pack8(yb);
-    }
+  for (int k = 0; k < 4; ++k) {
+    const float2 ua = __fmul2_rn(x.a[k], wa[k]), ub = __fmul2_rn(x.b[k], wb[k]);
+    ya[k] = f2_to_bf2(__fmul2_rn(__ffma2_rn(ua, c[k], __fmul2_rn(ub, ns[k])), iv));
+    yb[k] = f2_to_bf2(__fmul2_rn(__ffma2_rn(ub, c[k], __fmul2_rn(ua, s[k])), iv));
   }
+  *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(dst) + 16 * j) =
+      make_uint4(ya[0], ya[1], ya[2], ya[3]);
+  *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(dst) + D2 + 16 * j) =
+      make_uint4(yb[0], yb[1], yb[2], yb[3]);
 }
 
 // Stage layout: raw rows [Hq Q rows][Hkv K rows][Hkv V rows (D = 256 only)] of D bf16, then the
@@ -321,27 +279,25 @@ prep_kernel(PrepArgs a, int32_t nst, uint32_t stage_bytes) {
     }
   } else {
     // ---------------------------------------------------------------- consumers
-    // this lane's weights (Q and K), loaded once
-    float wq_lo[8], wq_hi[8], wk_lo[8], wk_hi[8];
-    if (D == 512) {
-      const int ci = lane * 8;
-      unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_q + ci)), wq_lo);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_k + ci)), wk_lo);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_q + 256 + ci)), wq_hi);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(a.w_k + 256 + ci)), wk_hi);
-    } else {
-      const int ci = lane * 4;
-      auto un4 = [](uint2 v, float* f) {
-        f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
-        f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
-      };
-      un4(__ldg(reinterpret_cast<const uint2*>(a.w_q + ci)), wq_lo);
-      un4(__ldg(reinterpret_cast<const uint2*>(a.w_k + ci)), wk_lo);
-      un4(__ldg(reinterpret_cast<const uint2*>(a.w_q + 128 + ci)), wq_hi);
-      un4(__ldg(reinterpret_cast<const uint2*>(a.w_k + 128 + ci)), wk_hi);
+    // LPR lanes per row: a warp holds 32 / LPR rows at a time (RPW), lane j = lane % LPR of
+    // row `sub` = lane / LPR. Rows are taken kind by kind (Q rows, then K rows, then the V rows
+    // of head_dim 256), RPW rows per warp at a time.
+    constexpr int LPR = D / 16, RPW = 32 / LPR, D2 = D;  // D2: bytes of half a row
+    const int j = lane % LPR, sub = lane / LPR;
+    const float inv_d = 1.0f / (float)D;
+    // this lane's weights (Q and K) as fp32 pairs, loaded once
+    float2 wqa[4], wqb[4], wka[4], wkb[4];
+    {
+      const uint4 qa = __ldg(reinterpret_cast<const uint4*>(a.w_q) + j);
+      const uint4 qb = __ldg(reinterpret_cast<const uint4*>(a.w_q + D / 2) + j);
+      const uint4 ka = __ldg(reinterpret_cast<const uint4*>(a.w_k) + j);
+      const uint4 kb = __ldg(reinterpret_cast<const uint4*>(a.w_k + D / 2) + j);
+      wqa[0] = bf2_to_f2(qa.x); wqa[1] = bf2_to_f2(qa.y); wqa[2] = bf2_to_f2(qa.z); wqa[3] = bf2_to_f2(qa.w);
+      wqb[0] = bf2_to_f2(qb.x); wqb[1] = bf2_to_f2(qb.y); wqb[2] = bf2_to_f2(qb.z); wqb[3] = bf2_to_f2(qb.w);
+      wka[0] = bf2_to_f2(ka.x); wka[1] = bf2_to_f2(ka.y); wka[2] = bf2_to_f2(ka.z); wka[3] = bf2_to_f2(ka.w);
+      wkb[0] = bf2_to_f2(kb.x); wkb[1] = bf2_to_f2(kb.y); wkb[2] = bf2_to_f2(kb.z); wkb[3] = bf2_to_f2(kb.w);
     }
-    // rotary column of this lane's first element
-    const int rc = D == 256 ? lane * 4 : lane * 8;
+    const int cw = warp;  // consumer warp index, 0..7
     for (int32_t k = 0; k < count; ++k) {
       const int st = k % nst;
       int okw = 1;
@@ -351,36 +307,53 @@ prep_kernel(PrepArgs a, int32_t nst, uint32_t stage_bytes) {
       const TokMeta m = *reinterpret_cast<const TokMeta*>(sg + hdr_off);
       if (m.ok) {
         const int32_t t = (int32_t)blockIdx.x + k * G;
-        float c[8], s[8];
+        // this token's rotary coefficients for the lane's 8 pairs
+        float2 c[4], sn[4], ns[4];
         {
-          const float4* cp = reinterpret_cast<const float4*>(sg + rows_bytes) + rc / 4;
-          const float4* sp = reinterpret_cast<const float4*>(sg + rows_bytes + D * 2) + rc / 4;
-          // D = 256 uses c[0..4), s[0..4) only
-          const float4 c0 = cp[0], c1 = D == 512 ? cp[1] : c0, s0 = sp[0], s1 = D == 512 ? sp[1] : s0;
-          c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
-          c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-          s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
-          s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+          const float4* cp = reinterpret_cast<const float4*>(sg + rows_bytes) + 2 * j;
+          const float4* sp = reinterpret_cast<const float4*>(sg + rows_bytes + D * 2) + 2 * j;
+          const float4 c0 = cp[0], c1 = cp[1], s0 = sp[0], s1 = sp[1];
+          c[0] = make_float2(c0.x, c0.y); c[1] = make_float2(c0.z, c0.w);
+          c[2] = make_float2(c1.x, c1.y); c[3] = make_float2(c1.z, c1.w);
+          sn[0] = make_float2(s0.x, s0.y); sn[1] = make_float2(s0.z, s0.w);
+          sn[2] = make_float2(s1.x, s1.y); sn[3] = make_float2(s1.z, s1.w);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ns[e] = make_float2(-sn[e].x, -sn[e].y);
         }
         __nv_bfloat16* const kbase = a.pool.layer_base + m.slot;
-        auto do_row = [&](int row) {
-          const int kind = row < Hq ? 0 : (row < Hq + Hkv ? 1 : 2);
-          __nv_bfloat16* dst;
-          __nv_bfloat16* vdst = nullptr;
-          if (kind == 0) {
-            dst = a.q_out + ((int64_t)t * Hq + row) * D;
-          } else if (kind == 1) {
-            dst = kbase + (int64_t)(row - Hq) * a.pool.stride_head;
-            vdst = dst + a.pool.stride_kv;
-          } else {
-            dst = kbase + a.pool.stride_kv + (int64_t)(row - Hq - Hkv) * a.pool.stride_head;
+        // Q rows
+        for (int r0 = cw * RPW; r0 < Hq; r0 += kPrepConsumerWarps * RPW) {
+          const int r = r0 + sub;
+          const bool live = r < Hq;
+          RowIn x;
+          const float inv = load_row<LPR>(sg + (size_t)(live ? r : r0) * (D * 2), j, D2, inv_d, a.eps, &x);
+          if (live)
+            store_rotated(x, inv, wqa, wqb, c, sn, ns, a.q_out + ((int64_t)t * Hq + r) * D, j, D2);
+        }
+        // K rows (head_dim 512: and the V row, the weightless norm of the same raw K)
+        for (int r0 = cw * RPW; r0 < Hkv; r0 += kPrepConsumerWarps * RPW) {
+          const int r = r0 + sub;
+          const bool live = r < Hkv;
+          RowIn x;
+          const float inv =
+              load_row<LPR>(sg + (size_t)(Hq + (live ? r : r0)) * (D * 2), j, D2, inv_d, a.eps, &x);
+          if (live) {
+            __nv_bfloat16* dst = kbase + (int64_t)r * a.pool.stride_head;
+            store_rotated(x, inv, wka, wkb, c, sn, ns, dst, j, D2);
+            if (D == 512) store_plain(x, inv, dst + a.pool.stride_kv, j, D2);
           }
-          if (kind == 0)
-            prep_row<D>(a, sg + (size_t)row * (D * 2), 0, lane, c, s, wq_lo, wq_hi, dst, vdst);
-          else
-            prep_row<D>(a, sg + (size_t)row * (D * 2), kind, lane, c, s, wk_lo, wk_hi, dst, vdst);
-        };
-        for (int row = warp; row < nrows; row += kPrepConsumerWarps) do_row(row);
+        }
+        // V rows of head_dim 256 (weightless, never rotated)
+        if (D == 256) {
+          for (int r0 = cw * RPW; r0 < Hkv; r0 += kPrepConsumerWarps * RPW) {
+            const int r = r0 + sub;
+            const bool live = r < Hkv;
+            RowIn x;
+            const float inv = load_row<LPR>(sg + (size_t)(Hq + Hkv + (live ? r : r0)) * (D * 2), j,
+                                            D2, inv_d, a.eps, &x);
+            if (live) store_plain(x, inv, kbase + a.pool.stride_kv + (int64_t)r * a.pool.stride_head, j, D2);
+          }
+        }
       }
       // every lane's shared-memory reads of this stage are done
       __syncwarp();
