@@ -81,7 +81,7 @@ constexpr float kHeadroomLog2 = 64.f;
 template <int DQK>
 struct TcCfg {
   static constexpr int KP = DQK / 256;                // K parts per tile (256 d each)
-  static constexpr int NKS = DQK == 256 ? 6 : 6;      // K part slots
+  static constexpr int NKS = DQK == 256 ? 5 : 6;      // K part slots
   static constexpr int NVR = DQK == 256 ? 6 : 3;      // V tile slots
   static constexpr int NS = NKS + NVR;
   static constexpr int QS_BYTES = (DQK - 256) * kM * 2;  // Q columns past 256, in shared memory
@@ -90,10 +90,17 @@ struct TcCfg {
   // writes P) and gives the 16 KB to the K ring
   static constexpr int NPB = DQK == 256 ? 2 : 1;
   static constexpr int SMEM_DATA = QS_BYTES + NS * kSlotBytes + NPB * P_BUF;
-  static constexpr int XL_BYTES = 2 * kM * 4;   // final row-sum exchange between warp pairs
-  static constexpr int NBAR = 2 * NS + 22;      // ..., QFREE, 4 per-producer fix-up barriers last
+  // final row-sum exchange between warp pairs; head_dim 256 also passes the rows' running
+  // reference from tile to tile ([tile parity][128 rows])
+  static constexpr int XM_FLOATS = DQK == 256 ? 2 * kM : 0;
+  static constexpr int XL_BYTES = 2 * kM * 4 + XM_FLOATS * 4;
+  // ..., QFREE, (head_dim 256: 8 reference handoffs), 4 per-producer fix-up barriers last
+  static constexpr int NBAR = 2 * NS + 22 + (DQK == 256 ? 8 : 0);
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
   static constexpr int NSB = 2;                 // S buffers (and PFULL / PVDONE barrier pairs)
+  // softmax warps (of both CTAs) that read each S buffer and write each P buffer: head_dim 256
+  // gives each tile to one warp of a lane quarter, head_dim 512 to both
+  static constexpr int SMW = DQK == 256 ? 8 : 16;
   static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384;
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -408,7 +415,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
                  PVDONE = SFULL + 56, QFULL = SFULL + 80, DRAIN = SFULL + 96,
                  PAIRB = SFULL + 104,  // 4 barriers, one per lane quarter
-                 QFREE = SFULL + 136;  // head_dim 512: the unit's QK MMAs have read Q's shared part
+                 QFREE = SFULL + 136,  // head_dim 512: the unit's QK MMAs have read Q's shared part
+                 PAIRX = SFULL + 144;  // head_dim 256: [tile parity][lane quarter] reference handoffs
   // ring slots, by the CTA's running tile count J: K part pp of tile J is the (J KP + pp)-th part
   // through the NKS K slots; V tile J uses V slot J mod NVR
   auto KSLOT = [&](int32_t j, int pp) { return (int)((j * KP + pp) % NKS); };
@@ -441,10 +449,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(SFULL + 8 * b, 1);
-      mbar_init(SFREE + 8 * b, 16);  // all softmax warps of both CTAs have read S
+      mbar_init(SFREE + 8 * b, C::SMW);  // the softmax warps of both CTAs that read S have
     }
     for (int b = 0; b < 3; ++b) {
-      mbar_init(PFULL + 8 * b, 16);
+      mbar_init(PFULL + 8 * b, C::SMW);
       mbar_init(PVDONE + 8 * b, 1);
     }
     // per unit: the sixteen softmax warps store Q columns [0,256) into TMEM; head_dim 512 also
@@ -454,6 +462,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int f = 0; f < 4; ++f) mbar_init(bars + 8u * (C::NBAR - 4 + f), 1);
     mbar_init(DRAIN, 2);  // one final commit from each MMA-issuing warp of the leader
     for (int q = 0; q < 4; ++q) mbar_init(PAIRB + 8 * q, 2);
+    if (DQK == 256)
+      for (int q = 0; q < 8; ++q) mbar_init(PAIRX + 8 * q, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -803,11 +813,159 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int32_t rlo = W >= 0 ? max(u.kv_start, prow - W) : u.kv_start;
       const int32_t rhi = min(prow + 1, u.kv_len);
       float m_ref = -INFINITY, l = 0.f;
+      if constexpr (DQK == 256) {
+        // Tile-parity softmax: the two warps of a lane quarter take alternate key tiles (warp h
+        // the tiles with JJ mod 2 == h, all 64 keys of each), so one warp's exponentials overlap
+        // the other's loads and maximum. The rows' running reference passes from tile to tile
+        // between the two warps through shared memory (hm[tile parity][row], one mbarrier per
+        // parity and quarter, bounded waits); each warp keeps its own partial row sum, and the
+        // two are brought to the unit's final reference and added at the end of the unit. The
+        // warp whose tile raises the reference rescales all of O's columns for its rows.
+        float* hm = xl + 2 * kM;  // [tile parity][row]
+        float m_mine = -INFINITY;  // the reference this warp's last tile used
+        for (int32_t j = 0; ok && j < ntiles; ++j) {
+          const int32_t JJ = J + j;
+          if ((JJ & 1) != h) continue;
+          const int b = JJ & 1;  // this warp's S and P buffers
+          if (!__all_sync(0xffffffffu, mbar_wait_inline(SFULL + 8 * b, (JJ >> 1) & 1, wc))) { ok = false; break; }
+          tc_fence_after();
+          uint32_t sv[kBN];
+          tmem_ld32(tl + kTmS + b * kBN, sv);
+          tmem_ld32(tl + kTmS + b * kBN + 32, sv + 32);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          // this warp has read S(JJ): the S buffer is free for QK(JJ + 2) once all have
+          if (lane == 0) mbar_arrive_cl(LEAD(SFREE + 8 * b));
+          const int32_t kb = u.kb0 + j * kBN;
+          const bool interior = __all_sync(0xffffffffu, rvalid && kb >= rlo && kb + kBN <= rhi);
+          if (!interior) {
+#pragma unroll
+            for (int k = 0; k < kBN; ++k) {
+              const int32_t key = kb + k;
+              const bool vis = rvalid && key >= rlo && key < rhi;
+              sv[k] = vis ? sv[k] : 0xFF800000u;  // -inf
+            }
+          }
+          // this tile's row maximum in log2 units; t holds the values the exponent scales
+          float t[kBN];
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          float mx;
+          const float tscale = a.scale_log2 > 0.f ? a.scale_log2 : 1.f;
+          if (a.scale_log2 > 0.f) {
+#pragma unroll
+            for (int k = 0; k < kBN; ++k) {
+              t[k] = __uint_as_float(sv[k]);
+              m4[k & 3] = fmaxf(m4[k & 3], t[k]);
+            }
+            mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBN; ++k) {
+              t[k] = sv[k] == 0xFF800000u ? -INFINITY : __uint_as_float(sv[k]) * a.scale_log2;
+              m4[k & 3] = fmaxf(m4[k & 3], t[k]);
+            }
+            mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          }
+          // the reference after the previous tile (the other warp's), then this tile's
+          float m_prev = -INFINITY;
+          if (j > 0) {
+            const int32_t jp = JJ - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_inline(PAIRX + 8 * ((jp & 1) * 4 + quarter), (jp >> 1) & 1, wc))) {
+              ok = false;
+              break;
+            }
+            m_prev = hm[(jp & 1) * kM + row];
+          }
+          // new reference with headroom above this maximum, so later growth rarely rescales
+          const float m_new = mx > m_prev + kRescaleLog2 ? mx + kHeadroomLog2 : m_prev;
+          hm[(JJ & 1) * kM + row] = m_new;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(PAIRX + 8 * ((JJ & 1) * 4 + quarter));
+          if (m_mine != m_new) {
+            if (m_mine != -INFINITY) l *= ex2(m_mine - m_new);
+            m_mine = m_new;
+          }
+          const float mu = m_new == -INFINITY ? 0.f : m_new;
+          uint32_t pk[kBN / 2];
+          {
+            // exponents and row sums on fp32 pairs; the row sum adds the bf16-rounded weights the
+            // PV product uses, so O / l is an exact weighted average of V rows
+            const float2 ts2 = make_float2(tscale, tscale), nmu2 = make_float2(-mu, -mu);
+            float2 sa = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kBN / 2; ++k) {
+              const float2 e = __ffma2_rn(make_float2(t[2 * k], t[2 * k + 1]), ts2, nmu2);
+              pk[k] = pack_bf16(ex2(e.x), ex2(e.y));
+              const float2 wv = make_float2(__uint_as_float(pk[k] << 16), __uint_as_float(pk[k] & 0xFFFF0000u));
+              if (k & 1) sb2 = __fadd2_rn(sb2, wv);
+              else sa = __fadd2_rn(sa, wv);
+            }
+            l += (sa.x + sb2.x) + (sa.y + sb2.y);
+          }
+          // P buffer b is free once PV(JJ - 2) has read it
+          if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ >> 1) & 1) ^ 1, wc))) { ok = false; break; }
+          {
+            // the row's 64 keys: eight 16-byte chunks of its 128-byte row, swizzled by the row
+            // within its 8-row atom
+            unsigned char* prow_p = gbase + (sP - base) + b * C::P_BUF + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(prow_p + ((c ^ (row & 7)) << 4)) =
+                  make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          }
+          // (after P is written, so the exponents' registers are free)
+          const bool resc = m_prev != -INFINITY && m_new != m_prev;
+          if (__any_sync(0xffffffffu, resc)) {
+            // O holds PV(0 .. JJ - 1) at the old reference: rescale all its columns before PV(JJ)
+            const float alpha = resc ? ex2(m_prev - m_new) : 1.f;
+            const int32_t jp = JJ - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jp % NSB), (jp / NSB) & 1, wc))) { ok = false; break; }
+            tc_fence_after();
+            for (int c = 0; c < kDV / 32; ++c) {
+              uint32_t o[32];
+              const uint32_t col = kTmO + c * 32;
+              tmem_ld32(tl + col, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(tl + col, o);
+            }
+            tmem_wait_st();
+          }
+          fence_proxy_async();  // the PV MMA reads P through the async proxy
+          tc_fence_before();    // and after any rescaling of O in TMEM above
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cl(LEAD(PFULL + 8 * b));
+        }
+        // the unit's final reference is its last tile's; this warp's partial sum follows it
+        if (ok && ntiles > 0) {
+          const int32_t jl = J + ntiles - 1;
+          float m_fin = m_mine;
+          if ((jl & 1) != h) {
+            if (!__all_sync(0xffffffffu, mbar_wait_inline(PAIRX + 8 * ((jl & 1) * 4 + quarter), (jl >> 1) & 1, wc)))
+              ok = false;
+            else
+              m_fin = hm[(jl & 1) * kM + row];
+          }
+          if (ok && m_fin != m_mine) {
+            if (m_mine != -INFINITY) l *= ex2(m_mine - m_fin);
+            m_mine = m_fin;
+          }
+        }
+        m_ref = m_mine;
+      } else {
       for (int32_t j = 0; ok && j < ntiles; ++j) {
         const int32_t JJ = J + j;
         const int b = JJ % NSB;
         if (!__all_sync(0xffffffffu, mbar_wait_inline(SFULL + 8 * b, (JJ / NSB) & 1, wc))) { ok = false; break; }
         tc_fence_after();
+        float mx;
+        // this thread's 32 keys (masked keys: -inf); log2 units are t * tscale
+        float t[HC];
+        const float tscale = a.scale_log2 > 0.f ? a.scale_log2 : 1.f;
+        const int32_t kb = u.kb0 + j * kBN;
+        {
         // both warps of the pair read the whole 64-key row: the row maximum needs no exchange
         uint32_t sv[kBN];
         tmem_ld32(tl + kTmS + b * kBN, sv);
@@ -817,7 +975,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         __syncwarp();
         // this warp has read S(JJ): the S buffer is free for QK(JJ + 2) once all have
         if (lane == 0) mbar_arrive_cl(LEAD(SFREE + 8 * b));
-        const int32_t kb = u.kb0 + j * kBN;
         const bool interior = __all_sync(0xffffffffu, rvalid && kb >= rlo && kb + kBN <= rhi);
         if (!interior) {
 #pragma unroll
@@ -828,10 +985,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        float mx;
-        // this thread's 32 keys (masked keys: -inf); log2 units are t * tscale
-        float t[HC];
-        const float tscale = a.scale_log2 > 0.f ? a.scale_log2 : 1.f;
         if (a.scale_log2 > 0.f) {
           // a positive scale keeps the maximum where it was, and masked keys at -inf
 #pragma unroll
@@ -849,6 +1002,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t v = h ? sv[HC + k] : sv[k];
             t[k] = v == 0xFF800000u ? -INFINITY : __uint_as_float(v) * a.scale_log2;
           }
+        }
         }
         float alpha = 1.f;
         bool resc = false;
@@ -876,16 +1030,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           tmem_wait_st();
         }
         const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[HC / 2];
+        {
+          // exponents and row sums on fp32 pairs; the row sum adds the bf16-rounded weights the
+          // PV product uses, so O / l is an exact weighted average of V rows (a dominant key's
+          // rounding cancels)
+          const float2 ts2 = make_float2(tscale, tscale), nmu2 = make_float2(-mu, -mu);
+          float2 sa = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < HC / 2; ++k) {
-          // the row sum adds the bf16-rounded weights the PV product uses, so O / l is an
-          // exact weighted average of V rows (a dominant key's rounding cancels)
-          pk[k] = pack_bf16(ex2(fmaf(t[2 * k], tscale, -mu)), ex2(fmaf(t[2 * k + 1], tscale, -mu)));
-          sum4[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+          for (int k = 0; k < HC / 2; ++k) {
+            const float2 e = __ffma2_rn(make_float2(t[2 * k], t[2 * k + 1]), ts2, nmu2);
+            pk[k] = pack_bf16(ex2(e.x), ex2(e.y));
+            const float2 w = make_float2(__uint_as_float(pk[k] << 16), __uint_as_float(pk[k] & 0xFFFF0000u));
+            if (k & 1) sb2 = __fadd2_rn(sb2, w);
+            else sa = __fadd2_rn(sa, w);
+          }
+          l += (sa.x + sb2.x) + (sa.y + sb2.y);
         }
-        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         // P buffer JJ mod NPB is free once PV(JJ - NPB) has read it
         if (C::NPB == 2) {
           if (!__all_sync(0xffffffffu, mbar_wait_inline(PVDONE + 8 * b, ((JJ / NSB) & 1) ^ 1, wc))) { ok = false; break; }
@@ -906,6 +1067,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_before();    // and after any rescaling of O in TMEM above
         __syncwarp();
         if (lane == 0) mbar_arrive_cl(LEAD(PFULL + 8 * b));
+      }
       }
       if (!ok) break;
       // the next unit's Q columns: this unit's QK MMAs are complete (every S was read)
