@@ -58,7 +58,7 @@ enum {
   PG_ERR_STREAM = -15,        /* call stream differs from the plan's stream ([P3] review)      */
   PG_ERR_CUDA = -16,          /* a CUDA runtime call failed                                    */
   PG_ERR_DEVICE_BOUNDS = -17, /* a kernel saw out-of-range metadata and skipped the access     */
-  PG_ERR_ALIGN = -18,         /* a device pointer or token stride breaks 16-byte alignment     */
+  PG_ERR_ALIGN = -18,         /* a device pointer or token stride breaks its stated alignment  */
   PG_ERR_DEVICE_TIMEOUT = -19 /* a kernel's bounded wait ran out; its outputs are not valid    */
 };
 
@@ -264,8 +264,8 @@ size_t pg_workspace_bytes(const pg_plan_t plan);
  * over keys j in [0, kv_len_r) with j <= p and (window_left < 0 or p - j <= window_left)
  * (inclusive distance: window_left + 1 keys), K_j / V_j read from pool `layer` through
  * the page table, KV head h / (Hq / Hkv). fp32 softmax, bf16 output (RNE).
- *   q   [T][Hq][256] bf16 contiguous (the prep's q_out)
- *   out [T][Hq][256] bf16 contiguous (written)
+ *   q   [T][Hq][256] bf16 contiguous, 32-byte aligned (the prep's q_out)
+ *   out [T][Hq][256] bf16 contiguous, 32-byte aligned (written)
  *   workspace: device scratch of ws_bytes >= pg_workspace_bytes(plan) (may be NULL when 0)
  * Checks (before launch): plan head_dim 256 and tile derivation, pool geometry, layer,
  * plan page bounds vs pool, window_left >= -1, sm_scale finite, workspace, alignment,

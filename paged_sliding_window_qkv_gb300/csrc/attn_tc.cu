@@ -10,13 +10,16 @@
 // outside the causal window. The kernel is persistent: one CTA per SM (its shared and tensor
 // memory fill the SM), each cluster taking one unit per round (longest first), so barriers,
 // tensor memory and K/V rings carry over from unit to unit: the producers fetch the next
-// unit's first tiles while the current one finishes, and the next unit's Q enters TMEM before
-// this unit's epilogue.
+// unit's first tiles while the current one finishes, the next unit's Q enters TMEM before
+// this unit's epilogue, and the next unit's first PV waits only for every softmax warp's read
+// of O.
 //
 //   warp 0     K producer (TMA): this CTA's 32 keys of each tile, one 4-D box per page
 //              (BR rows x 256 d) into 16 KB part slots; box coordinates and page ids are
 //              worked out a batch of tiles ahead, and a head_dim 512 tile's two parts go out
-//              in one copy instruction; also each unit's Q columns [256,512) (head_dim 512)
+//              in one copy instruction; also Q into shared memory: head_dim 512 each unit's
+//              columns [256,512), head_dim 256 the whole of the next unit's Q (staged while
+//              this unit runs, so Q's reads do not fall in the unit transition)
 //   warp 10    V producer (TMA): this CTA's 128 output columns of each tile, one 3-D box per
 //              page into 16 KB slots
 //   warp 1     QK issuer (leader CTA): S = Q K^T into a TMEM S buffer (2-SM MMA, M=256, N=64,
@@ -25,13 +28,18 @@
 //   warp 11    PV issuer (leader CTA): O += P V into TMEM (M=256, N=256, K=16 steps; P from
 //              shared memory); MMAs are issued by lane 0, completion signalled with
 //              tcgen05.commit multicast to both CTAs
-//   warps 2..9 softmax: the unit's first Q columns [0,256) into TMEM; then two threads per
-//              query row (each reads the whole S row for the maximum, exponentiates half of
-//              the tile's keys and owns half of O's columns), masked on boundary tiles only,
-//              online softmax in log2 units with lazy rescaling (O is rescaled in TMEM only
-//              when a row maximum outgrows a 2^64 headroom by more than 2^48: bf16 P and fp32
-//              O and row sums hold the range, and O / l is unchanged); then the epilogue
-//              normalises O and each thread stores its 256 contiguous bytes of the row.
+//   warps 2..9 softmax: two warps per TMEM lane quarter (32 query rows), masked on boundary
+//              tiles only, online softmax in log2 units with lazy rescaling (O is rescaled in
+//              TMEM only when a row maximum outgrows a 2^64 headroom by more than 2^48: bf16 P
+//              and fp32 O and row sums hold the range, and O / l is unchanged). head_dim 256:
+//              the two warps take alternate key tiles (all 64 keys each), pass the rows'
+//              running reference between them, and the one that takes the next unit's first
+//              tile moves that unit's staged Q into TMEM while the other finishes the last
+//              tile; the epilogue passes each warp's 32 rows x 128 output columns through its
+//              quarter of its P buffer to coalesced 16-byte stores. head_dim 512: both warps read every
+//              tile, each exponentiates half of its keys, each stores half of the next unit's
+//              first Q part, and the epilogue stores 256 contiguous bytes of a row per thread.
+//              Each thread owns half of its row's O columns.
 //
 // O holds 256 output columns: for head_dim 512 each query tile is two units, each computing
 // the full 512-wide S and half of O. The TMEM map is described at TcCfg.
@@ -76,15 +84,19 @@ constexpr float kHeadroomLog2 = 64.f;
 // [256,384) (this unit's first 256-d part of Q; QK reads A from TMEM), two S buffers
 // [384,448) and [448,512). The softmax writes P(j) to a 16 KB shared-memory buffer (NPB of
 // them; PV is SS), so QK(j + 2) waits only for both CTAs' reads of S(j). head_dim 512 also keeps Q
-// columns [256,512) in shared memory (64 KB; QK's second part is SS). K streams through NKS
-// 256-d part slots (a tile is KP parts), V through NVR tile slots.
+// columns [256,512) in shared memory (64 KB; QK's second part is SS); head_dim 256 uses the same
+// 64 KB to stage the next unit's Q. K streams through NKS 256-d part slots (a tile is KP parts),
+// V through NVR tile slots.
 template <int DQK>
 struct TcCfg {
   static constexpr int KP = DQK / 256;                // K parts per tile (256 d each)
-  static constexpr int NKS = DQK == 256 ? 5 : 6;      // K part slots
-  static constexpr int NVR = DQK == 256 ? 6 : 3;      // V tile slots
+  static constexpr int NKS = DQK == 256 ? 3 : 6;      // K part slots
+  static constexpr int NVR = DQK == 256 ? 4 : 3;      // V tile slots
   static constexpr int NS = NKS + NVR;
-  static constexpr int QS_BYTES = (DQK - 256) * kM * 2;  // Q columns past 256, in shared memory
+  // 128 rows x 256 d of Q in shared memory: head_dim 512 keeps the unit's Q columns [256,512)
+  // there (QK's second part reads them); head_dim 256 stages the next unit's Q there, loaded by
+  // TMA during this unit and moved into TMEM at the unit's end
+  static constexpr int QS_BYTES = kM * 256 * 2;
   static constexpr int P_BUF = kM * kBN * 2;          // one P buffer: 128 rows x 64 keys bf16
   // P buffers: head_dim 512 keeps one (PV(j) has long completed when the softmax of tile j + 1
   // writes P) and gives the 16 KB to the K ring
@@ -94,8 +106,9 @@ struct TcCfg {
   // reference from tile to tile ([tile parity][128 rows])
   static constexpr int XM_FLOATS = DQK == 256 ? 2 * kM : 0;
   static constexpr int XL_BYTES = 2 * kM * 4 + XM_FLOATS * 4;
-  // ..., QFREE, (head_dim 256: 8 reference handoffs), 4 per-producer fix-up barriers last
-  static constexpr int NBAR = 2 * NS + 22 + (DQK == 256 ? 8 : 0);
+  // ..., QFREE, (head_dim 256: 8 reference handoffs, Q staging full / free), 4 per-producer
+  // fix-up barriers last
+  static constexpr int NBAR = 2 * NS + 22 + (DQK == 256 ? 10 : 0);
   static constexpr int SMEM = SMEM_DATA + XL_BYTES + NBAR * 8 + 16 + 1024;
   static constexpr int NSB = 2;                 // S buffers (and PFULL / PVDONE barrier pairs)
   // softmax warps (of both CTAs) that read each S buffer and write each P buffer: head_dim 256
@@ -413,10 +426,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   // leader only and count both CTAs' arrivals; EMPTY, SFULL, PVDONE, QFREE and DRAIN receive
   // the leader's commits in both CTAs; PAIRB and the fix-up barriers are local.
   const uint32_t SFULL = bars + 8u * (2 * NS), SFREE = SFULL + 16, PFULL = SFULL + 32,
-                 PVDONE = SFULL + 56, QFULL = SFULL + 80, DRAIN = SFULL + 96,
+                 PVDONE = SFULL + 56, QFULL = SFULL + 80,
+                 OFREE = SFULL + 88,  // head_dim 256: every softmax warp has read the unit's O
+                 DRAIN = SFULL + 96,
                  PAIRB = SFULL + 104,  // 4 barriers, one per lane quarter
                  QFREE = SFULL + 136,  // head_dim 512: the unit's QK MMAs have read Q's shared part
-                 PAIRX = SFULL + 144;  // head_dim 256: [tile parity][lane quarter] reference handoffs
+                 PAIRX = SFULL + 144,  // head_dim 256: [tile parity][lane quarter] reference handoffs
+                 QSFULL = SFULL + 208,  // head_dim 256: the next unit's Q has landed in shared memory
+                 QSFREE = SFULL + 216;  // head_dim 256: ... and has been moved into TMEM
   // ring slots, by the CTA's running tile count J: K part pp of tile J is the (J KP + pp)-th part
   // through the NKS K slots; V tile J uses V slot J mod NVR
   auto KSLOT = [&](int32_t j, int pp) { return (int)((j * KP + pp) % NKS); };
@@ -455,15 +472,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(PFULL + 8 * b, C::SMW);
       mbar_init(PVDONE + 8 * b, 1);
     }
-    // per unit: the sixteen softmax warps store Q columns [0,256) into TMEM; head_dim 512 also
-    // loads the rest of each CTA's Q by TMA
-    mbar_init(QFULL, C::QS_BYTES > 0 ? 18 : 16);
+    // per unit: head_dim 256: the four softmax warps of each CTA that take the unit's first tile
+    // store its Q into TMEM; head_dim 512: all sixteen store Q columns [0,256), and each CTA's
+    // K producer loads the rest by TMA
+    mbar_init(QFULL, DQK == 256 ? 8 : 18);
+    mbar_init(OFREE, 16);
     mbar_init(QFREE, 1);
     for (int f = 0; f < 4; ++f) mbar_init(bars + 8u * (C::NBAR - 4 + f), 1);
     mbar_init(DRAIN, 2);  // one final commit from each MMA-issuing warp of the leader
     for (int q = 0; q < 4; ++q) mbar_init(PAIRB + 8 * q, 2);
-    if (DQK == 256)
+    if (DQK == 256) {
       for (int q = 0; q < 8; ++q) mbar_init(PAIRX + 8 * q, 1);
+      mbar_init(QSFULL, 1);  // the K producer's arrival with the staged bytes
+      mbar_init(QSFREE, 4);  // the four softmax warps (one per lane quarter) that move it
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -500,21 +522,40 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int key_off = is_v ? 0 : (int)rank * kKH;      // this CTA's first key of a tile
     const uint32_t row_bytes = is_v ? 256u : 512u;       // bytes of one key row in a slot
     const int64_t head_rows = (int64_t)ps;
+    // head_dim 256: Q of the cluster's k-th unit goes into the staging buffer once the softmax
+    // warps have moved Q of unit k - 1 out of it (QSFREE phase k - 1); one lane issues it
+    auto stage_q = [&](int32_t k) -> bool {
+      if (lane != 0) return true;
+      if (k > 0 && !mbar_wait(QSFREE, (k - 1) & 1, wc)) return false;
+      const TcUnit v = tc_unit(a, unit_at(k), NDH, (int32_t)rank);
+      mbar_expect_tx(QSFULL, v.ntok > 0 ? (uint32_t)C::QS_BYTES : 0u);
+      if (v.ntok > 0)
+        for (int c = 0; c < 4; ++c)
+          tma_load_3d(sQ + c * (kM * 128), &tm_q, c * 64, v.g * G, v.q0 + v.tok0, mapa(QSFULL, rank));
+      return true;
+    };
+    if (DQK == 256 && !is_v && unit_at(0) < nunits) ok = __shfl_sync(0xffffffffu, stage_q(0) ? 1 : 0, 0) != 0;
     int32_t J = 0;  // tiles of this cluster's earlier units
     int32_t ui = 0;
     for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
       const TcUnit u = tc_unit(a, w, NDH, (int32_t)rank);
+      // head_dim 256: the next unit's Q is staged after this unit's fourth K tile has been issued:
+      // that tile's slot wait shows this unit's first QK complete, so its Q has left the staging
+      // buffer and the wait for it does not hold up the ring (in units of up to four tiles it
+      // comes after the last tile)
+      const bool stage_next = DQK == 256 && !is_v && unit_at(ui + 1) < nunits;
+      const int32_t stage_at = min(u.ntiles, 4);
       if (!is_v && lane == 0) {
         // a unit ahead, bring the next unit's pair-table entry and this CTA's Q rows of it into
         // L2, so the softmax warps' move to that unit waits on L2 rather than DRAM
         if (unit_at(ui + 2) < nunits) tc_unit_prefetch(a, unit_at(ui + 2), NDH);
-        if (unit_at(ui + 1) < nunits) {
+        if (DQK != 256 && unit_at(ui + 1) < nunits) {
           const TcUnit un = tc_unit(a, unit_at(ui + 1), NDH, (int32_t)rank);
           if (un.ntok > 0)
             for (int c = 0; c < DQK / 64; ++c) tma_prefetch_3d(&tm_q, c * 64, un.g * G, un.q0 + un.tok0);
         }
       }
-      if (C::QS_BYTES > 0 && !is_v) {
+      if (DQK == 512 && !is_v) {
         // Q columns [256,512) of this CTA's tile, once the previous unit's QK MMAs have read them
         int go = 1;
         if (lane == 0) {
@@ -554,6 +595,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const uint32_t box_bytes = (uint32_t)BR * row_bytes;
       for (int32_t t = 0; ok && t < u.ntiles; ++t) {
         const int32_t JJ = J + t;
+        if (stage_next && t == stage_at && !__shfl_sync(0xffffffffu, stage_q(ui + 1) ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
         const int tb = t % TB;
         if (tb == 0) {
           my_page = pg_next;
@@ -657,6 +702,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
       }
+      if (ok && stage_next && stage_at == u.ntiles)
+        ok = __shfl_sync(0xffffffffu, stage_q(ui + 1) ? 1 : 0, 0) != 0;
       J += u.ntiles;
     }
     if (!ok) {
@@ -680,6 +727,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     bool ok = true;
     int32_t J = 0;  // tiles of this cluster's earlier units
     int32_t ui = 0;
+    int32_t nof = 0;  // head_dim 256: units with tiles whose PVs this warp has issued
     for (int32_t w = unit_at(0); leader && ok && w < nunits; w = unit_at(++ui)) {
       const int32_t ntiles = tc_unit(a, w, NDH, 0).ntiles;
       if (warp == 1) {
@@ -725,10 +773,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           mma_commit(SFULL + 8 * sb);
         }
         // Q's shared-memory parts may be replaced once this unit's QK MMAs have completed
-        if (ok && C::QS_BYTES > 0) mma_commit(QFREE);
+        if (ok && DQK == 512) mma_commit(QFREE);
       } else {
         const int BR = a.box_rows_v;
         const uint32_t lbo = (uint32_t)BR * 128u, sbo = BR >= 16 ? 1024u : (uint32_t)BR * 256u;
+        if (DQK == 256 && ntiles > 0) {
+          // the unit's first PV starts O afresh: only once every softmax warp (both CTAs) has
+          // read the previous unit's O (a tile's P comes from one warp of each pair here, so
+          // PFULL alone does not say that the other warp's epilogue is done)
+          if (nof > 0) ok = wait1(OFREE, (nof - 1) & 1);
+          ++nof;
+        }
         for (int32_t jp = 0; ok && jp < ntiles; ++jp) {
           const int32_t JJ = J + jp;
           const int pb = JJ % NSB;
@@ -771,12 +826,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint32_t pair_phase = 0;
     bool ok = true;
     constexpr int HC = kBN / 2;  // key columns per half
-    // Q rows into TMEM: this thread stores its row's d columns [128h, 128h + 128) as bf16
-    // pairs (64 TMEM columns), the A operand layout of QK
-    auto store_q = [&](const TcUnit& v) {
+    // head_dim 256: this warp's quarter of its own P buffer (its 32 rows x 128 bytes, rows
+    // 128-byte swizzled) is free between its P writes and serves to transpose the epilogue's
+    // output from the row-per-lane layout of TMEM to coalesced global stores (eight lanes per
+    // 128-byte piece of a row, four rows per instruction: lane l takes row 4 i + l / 8, piece
+    // l mod 8).
+    unsigned char* const tbuf = gbase + (sP - base) + h * C::P_BUF + quarter * 4096;
+    const int crow = lane >> 3, cpc = lane & 7;
+    // G divides the 128 rows of a tile, so it is a power of two: rows split into (token, head)
+    // by shift and mask
+    const int gsh = __ffs(G) - 1;
+    const int32_t gmask = G - 1;
+    // Q rows into TMEM (bf16 pairs, the A operand layout of QK). head_dim 512: this warp's d
+    // columns [128h, 128h + 128) of the first 256-d part, one 32-byte load per row and lane.
+    auto load_q128 = [&](const TcUnit& v, int d0) {
       const bool valid = row < v.ntok * G;
       const uint4* src = reinterpret_cast<const uint4*>(
-          a.q + ((int64_t)(v.q0 + v.tok0 + row / G) * Hq + v.g * G + row % G) * DQK + h * 128);
+          a.q + ((int64_t)(v.q0 + v.tok0 + (row >> gsh)) * Hq + v.g * G + (row & gmask)) * DQK + d0);
       // all loads in flight before the first store; 32-byte loads halve the instructions, each
       // of which touches 32 rows (one per lane)
       uint32_t w[64];
@@ -792,24 +858,63 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           for (int e = 0; e < 8; ++e) w[8 * q + e] = 0u;
         }
       }
-      tmem_st32(tl + kTmQ + h * 64, w);
-      tmem_st32(tl + kTmQ + h * 64 + 32, w + 32);
+      tmem_st32(tl + kTmQ + d0 / 2, w);
+      tmem_st32(tl + kTmQ + d0 / 2 + 32, w + 32);
       tmem_wait_st();
+    };
+    // head_dim 256: Q of the cluster's k-th unit from the staging buffer (TMA-written as four
+    // 64-d pieces of [128 rows][128 swizzled bytes]) into TMEM, this warp's 32 rows; then the
+    // buffer is released to the K producer
+    auto copy_q256 = [&](int32_t k) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(QSFULL, k & 1, wc))) return false;
+      const unsigned char* src = gbase + (sQ - base) + row * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 y = *reinterpret_cast<const uint4*>(src + c * (kM * 128) + ((q ^ (row & 7)) << 4));
+          w[4 * q] = y.x;
+          w[4 * q + 1] = y.y;
+          w[4 * q + 2] = y.z;
+          w[4 * q + 3] = y.w;
+        }
+        tmem_st32(tl + kTmQ + c * 32, w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(QSFREE);
+      tmem_wait_st();
+      return true;
+    };
+    auto q_stored = [&]() {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cl(LEAD(QFULL));
+    };
+    // head_dim 256: the warp of each pair that takes the unit's first tile moves all 256 Q
+    // columns of the cluster's k-th unit in from the staging buffer; head_dim 512: each warp
+    // loads its 128 columns of Q's first part
+    auto store_q = [&](const TcUnit& v, int32_t k) -> bool {
+      tc_fence_after();  // after the wait that showed the previous QK MMAs complete
+      if (DQK == 256) {
+        if (!copy_q256(k)) return false;
+      } else {
+        load_q128(v, h * 128);
+      }
+      q_stored();
+      return true;
     };
     int32_t J = 0;  // tiles of this cluster's earlier units
     TcUnit u;
     int32_t ui = 0;
     if (unit_at(0) < nunits) {
       u = tc_unit(a, unit_at(0), NDH, (int32_t)rank);
-      store_q(u);
+      if (DQK != 256 || h == 0) ok = store_q(u, 0);
     }
     for (int32_t w = unit_at(0); ok && w < nunits; w = unit_at(++ui)) {
       const int32_t ntiles = u.ntiles;
       const bool rvalid = row < u.ntok * G;
-      const int32_t prow = u.sp + u.tok0 + row / G;
+      const int32_t prow = u.sp + u.tok0 + (row >> gsh);
       const int32_t rlo = W >= 0 ? max(u.kv_start, prow - W) : u.kv_start;
       const int32_t rhi = min(prow + 1, u.kv_len);
       float m_ref = -INFINITY, l = 0.f;
@@ -1070,67 +1175,139 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       }
       if (!ok) break;
-      // the next unit's Q columns: this unit's QK MMAs are complete (every S was read)
       const int32_t wn = unit_at(ui + 1);
       TcUnit un;
-      if (wn < nunits) {
-        un = tc_unit(a, wn, NDH, (int32_t)rank);
-        store_q(un);
-      }
-      if (ntiles > 0) {
+      if (wn < nunits) un = tc_unit(a, wn, NDH, (int32_t)rank);
+      if constexpr (DQK == 256) {
+        // The row sum is the sum of the two warps' partial sums, swapped through shared memory.
+        // The warp that wrote the last tile's P waits for that tile's PV before publishing (its
+        // own earlier waits keep that PVDONE barrier at most a phase behind); the other warp
+        // publishes at once, so the partner's epilogue does not wait for its Q load, and waits
+        // for the last PV after the exchange (before it, the barrier of the other parity can be
+        // two phases behind this warp's view and a parity wait would pass early). A warp has
+        // read the partner's value before the partner writes its next one: that write follows
+        // the next unit's first PV, or the other warp's next tile, and both wait for this
+        // warp's epilogue (OFREE, the reference handoff).
         const int32_t jl = J + ntiles - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, wc));
-        // the row sum is the sum of both halves' partial sums, swapped through shared memory.
-        // The partner has read this unit's value before this warp writes the next one: that
-        // write waits for the next unit's last PV, which needs the partner's P of that tile,
-        // which it writes after this unit's epilogue.
-        if (ok) {
+        const bool last = ntiles > 0 && (jl & 1) == h;
+        if (last) ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, wc));
+        if (ok && ntiles > 0) {
           xl[h * kM + row] = l;
           __syncwarp();
           if (lane == 0) mbar_arrive(pair_bar);
+        }
+        // The warp that takes the next unit's first tile stores its Q now: this unit's QK MMAs
+        // have completed, since that warp has seen the last tile's S through the reference
+        // handoff (or, in a unit without tiles, at the end of an earlier unit).
+        if (ok && wn < nunits && ((J + ntiles) & 1) == h) ok = store_q(un, ui + 1);
+        if (ok && ntiles > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, wc));
           pair_phase ^= 1u;
+          if (ok && !last) ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, wc));
           if (ok) l = xl[row] + xl[kM + row];
+        }
+      } else {
+        // the next unit's Q columns: this unit's QK MMAs are complete (every S was read)
+        if (wn < nunits) store_q(un, ui + 1);
+        if (ntiles > 0) {
+          const int32_t jl = J + ntiles - 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(PVDONE + 8 * (jl % NSB), (jl / NSB) & 1, wc));
+          // the row sum is the sum of both halves' partial sums, swapped through shared memory.
+          // The partner has read this unit's value before this warp writes the next one: that
+          // write waits for the next unit's last PV, which needs the partner's P of that tile,
+          // which it writes after this unit's epilogue.
+          if (ok) {
+            xl[h * kM + row] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair_bar);
+            ok = __all_sync(0xffffffffu, mbar_wait(pair_bar, pair_phase, wc));
+            pair_phase ^= 1u;
+            if (ok) l = xl[row] + xl[kM + row];
+          }
         }
       }
       if (ok) {
-        // epilogue: normalise this thread's 128 output columns and store them (256 contiguous
-        // bytes of the row)
+        // epilogue: normalise this thread's 128 output columns [128h, 128h + 128) of the row
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         if (a.lse && rvalid && h == 0 && u.dh == 0)  // both output halves of hd512 agree
-          a.lse[(int64_t)(u.q0 + u.tok0 + row / G) * Hq + u.g * G + row % G] =
+          a.lse[(int64_t)(u.q0 + u.tok0 + (row >> gsh)) * Hq + u.g * G + (row & gmask)] =
               l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-        __nv_bfloat16* dst = a.out + ((int64_t)(u.q0 + u.tok0 + row / G) * Hq + u.g * G + row % G) * DQK +
-                             u.dh * kDV + h * (kDV / 2);
-        for (int c2 = 0; c2 < kDV / 64; c2 += 2) {
-          // two 32-column loads in flight per wait
-          uint32_t o[64];
-          tmem_ld32(tl + kTmO + h * (kDV / 2) + c2 * 32, o);
-          tmem_ld32(tl + kTmO + h * (kDV / 2) + c2 * 32 + 32, o + 32);
-          tmem_wait_ld();
-          if (rvalid) {
+        if (DQK == 256) {
+          // each 64-column half of this warp's 128 columns goes through the transposition
+          // buffer (free: every PV of the unit has completed) and out in coalesced 16-byte
+          // stores, four rows per instruction; rows past the tile's tokens are not written
+          const int32_t nvalid = u.ntok * G;
+          __nv_bfloat16* const obase = a.out + (int64_t)(u.q0 + u.tok0) * Hq * DQK + (int64_t)u.g * G * DQK +
+                                       u.dh * kDV + h * (kDV / 2) + cpc * 8;
+#pragma unroll 1
+          for (int bx = 0; bx < 2; ++bx) {
+            uint32_t wv[32];
+            if (ntiles > 0) {
+              uint32_t o[64];
+              tmem_ld32(tl + kTmO + h * (kDV / 2) + bx * 64, o);
+              tmem_ld32(tl + kTmO + h * (kDV / 2) + bx * 64 + 32, o + 32);
+              tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint32_t wv[16];
+              for (int e = 0; e < 32; ++e)
+                wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+            } else {
 #pragma unroll
-              for (int e = 0; e < 16; ++e)
-                wv[e] = ntiles == 0 ? 0u
-                                    : pack_bf16(__uint_as_float(o[32 * c + 2 * e]) * inv,
-                                                __uint_as_float(o[32 * c + 2 * e + 1]) * inv);
-              // 32-byte stores: each instruction touches 32 rows (one per lane)
-              __nv_bfloat16* d = dst + (c2 + c) * 32;
+              for (int e = 0; e < 32; ++e) wv[e] = 0u;
+            }
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh)
-                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d + 16 * hh),
-                             "r"(wv[8 * hh]), "r"(wv[8 * hh + 1]), "r"(wv[8 * hh + 2]), "r"(wv[8 * hh + 3]),
-                             "r"(wv[8 * hh + 4]), "r"(wv[8 * hh + 5]), "r"(wv[8 * hh + 6]), "r"(wv[8 * hh + 7])
-                             : "memory");
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<uint4*>(tbuf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                  make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + crow;
+              const int32_t R = quarter * 32 + r;
+              if (R < nvalid) {
+                const uint4 x = *reinterpret_cast<const uint4*>(tbuf + r * 128 + ((cpc ^ (r & 7)) << 4));
+                *reinterpret_cast<uint4*>(obase + ((int64_t)(R >> gsh) * Hq + (R & gmask)) * DQK + bx * 64) = x;
+              }
+            }
+            __syncwarp();  // read before the next half overwrites the buffer
+          }
+        } else {
+          // head_dim 512: 256 contiguous bytes of the row per thread
+          __nv_bfloat16* dst = a.out + ((int64_t)(u.q0 + u.tok0 + (row >> gsh)) * Hq + u.g * G + (row & gmask)) * DQK +
+                               u.dh * kDV + h * (kDV / 2);
+          for (int c2 = 0; c2 < kDV / 64; c2 += 2) {
+            // two 32-column loads in flight per wait
+            uint32_t o[64];
+            tmem_ld32(tl + kTmO + h * (kDV / 2) + c2 * 32, o);
+            tmem_ld32(tl + kTmO + h * (kDV / 2) + c2 * 32 + 32, o + 32);
+            tmem_wait_ld();
+            if (rvalid) {
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                uint32_t wv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  wv[e] = ntiles == 0 ? 0u
+                                      : pack_bf16(__uint_as_float(o[32 * c + 2 * e]) * inv,
+                                                  __uint_as_float(o[32 * c + 2 * e + 1]) * inv);
+                // 32-byte stores: each instruction touches 32 rows (one per lane)
+                __nv_bfloat16* d = dst + (c2 + c) * 32;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d + 16 * hh),
+                               "r"(wv[8 * hh]), "r"(wv[8 * hh + 1]), "r"(wv[8 * hh + 2]), "r"(wv[8 * hh + 3]),
+                               "r"(wv[8 * hh + 4]), "r"(wv[8 * hh + 5]), "r"(wv[8 * hh + 6]), "r"(wv[8 * hh + 7])
+                               : "memory");
+              }
             }
           }
         }
         // the next unit's first PV overwrites O only after these reads
         tc_fence_before();
+        if (DQK == 256 && ntiles > 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cl(LEAD(OFREE));
+        }
       }
       J += ntiles;
       u = un;

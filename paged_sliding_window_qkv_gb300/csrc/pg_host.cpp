@@ -432,7 +432,8 @@ int attn_common(const pg_plan* plan, const pg_pool_t* pool, int32_t layer, int32
     return PG_ERR_I32_OVERFLOW;  // tensor-map row coordinates are int32
   if (plan->num_tokens == 0) return PG_OK;
   if (!q || !out) return PG_ERR_ARG;
-  if (!aligned16(q) || !aligned16(out)) return PG_ERR_ALIGN;
+  // the tensor-core prefill kernel reads Q rows and writes output rows in 32-byte accesses
+  if ((((uintptr_t)q | (uintptr_t)out) & 31u) != 0) return PG_ERR_ALIGN;
   if (lse && ((uintptr_t)lse & 3u) != 0) return PG_ERR_ALIGN;
   const size_t need = workspace_bytes(plan);
   if (need > 0) {
