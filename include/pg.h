@@ -107,9 +107,13 @@ typedef struct {
  * prep and attention compare them with the pool before every launch.
  *
  * Device metadata is uploaded on `stream`; the plan is bound to that stream and later
- * calls on another stream fail with PG_ERR_STREAM. An update builds and uploads into
- * fresh storage and replaces the plan only on success: on any error the plan is left
- * exactly as it was. num_req == 0 is a valid empty plan (calls launch nothing).
+ * calls on another stream fail with PG_ERR_STREAM. An update checks every input on the
+ * host before anything changes: on any error the plan is left exactly as it was. The
+ * metadata then goes through a pinned host staging buffer of the plan (the call does not
+ * wait for the stream) into the plan's device storage, in place when it is large enough
+ * (ordered after every call already queued on the stream, which read the old metadata;
+ * a CUDA graph that captured the plan's calls reads the new), else into fresh storage that
+ * replaces the old. num_req == 0 is a valid empty plan (calls launch nothing).
  */
 int pg_plan_paged_prefill(pg_plan_t* plan, int32_t num_req, const int64_t* qo_indptr,
                           const int64_t* kv_page_indptr, const int32_t* page_ids,

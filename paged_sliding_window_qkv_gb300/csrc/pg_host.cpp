@@ -72,6 +72,17 @@ static int32_t plan_kv_chunk(int32_t head_dim) { return head_dim == 512 ? 512 : 
 
 using namespace pg;
 
+// Pinned host staging for a plan's metadata upload, two buffers used alternately: an upload from
+// pageable memory can hold the host until the stream reaches it, which in a serving loop that
+// rebuilds a plan while earlier calls still run would stall every later launch. Buffer k is
+// rewritten only after the upload recorded on done[k] (two builds back) has completed.
+struct PlanStage {
+  int32_t* host[2] = {nullptr, nullptr};
+  size_t cap[2] = {0, 0};
+  cudaEvent_t done[2] = {nullptr, nullptr};
+  int next = 0;
+};
+
 struct pg_plan {
   int32_t num_req = 0, num_tokens = 0, num_qo_heads = 0, num_kv_heads = 0, head_dim = 0,
           page_size = 0;
@@ -87,12 +98,28 @@ struct pg_plan {
   int device = 0;
   int32_t* dev = nullptr;  // one device allocation holding every metadata array
   size_t dev_elems = 0;
+  size_t dev_cap = 0;      // bytes allocated at dev
   // offsets (elements) of each array inside `dev`
   size_t o_qo = 0, o_kvp = 0, o_pages = 0, o_last = 0, o_start = 0, o_kvs = 0, o_tokreq = 0,
          o_wreq = 0, o_wtok = 0, o_pair = 0;
+  PlanStage stage;  // carried over from build to build of the same plan
 };
 
 namespace {
+
+// releases a plan's staging buffers once their uploads have completed
+void free_stage(PlanStage* st) {
+  for (int k = 0; k < 2; ++k) {
+    if (st->done[k]) {
+      cudaEventSynchronize(st->done[k]);
+      cudaEventDestroy(st->done[k]);
+      st->done[k] = nullptr;
+    }
+    if (st->host[k]) cudaFreeHost(st->host[k]);
+    st->host[k] = nullptr;
+    st->cap[k] = 0;
+  }
+}
 
 // ring_window < 0: linear addressing (slot = position, pages cover [0, kv_len) exactly, with
 // last_page_len). ring_window >= 0: ring addressing for window-crossing requests: logical page
@@ -246,14 +273,46 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   if (!status_word(&err)) return err;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PG_ERR_CUDA;
-  int32_t* d = nullptr;
-  if (cudaMallocAsync((void**)&d, host.size() * sizeof(int32_t), stream) != cudaSuccess)
-    return PG_ERR_CUDA;
-  if (cudaMemcpyAsync(d, host.data(), host.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
-                      stream) != cudaSuccess) {
-    cudaFreeAsync(d, stream);
+  // the upload goes through this plan's next pinned staging buffer (see PlanStage)
+  PlanStage& st = p->stage;
+  const int k = st.next;
+  const size_t bytes = host.size() * sizeof(int32_t);
+  if (!st.done[k]) {
+    if (cudaEventCreateWithFlags(&st.done[k], cudaEventDisableTiming) != cudaSuccess) {
+      st.done[k] = nullptr;
+      return PG_ERR_CUDA;
+    }
+  } else if (cudaEventSynchronize(st.done[k]) != cudaSuccess) {
     return PG_ERR_CUDA;
   }
+  if (st.cap[k] < bytes) {
+    if (st.host[k]) cudaFreeHost(st.host[k]);
+    st.host[k] = nullptr;
+    st.cap[k] = 0;
+    if (cudaMallocHost((void**)&st.host[k], bytes) != cudaSuccess) {
+      st.host[k] = nullptr;
+      return PG_ERR_CUDA;
+    }
+    st.cap[k] = bytes;
+  }
+  std::memcpy(st.host[k], host.data(), bytes);
+  // An existing plan whose device storage is large enough is updated in place: the copy is
+  // ordered on the plan's stream after every call already queued with the old metadata (a plan
+  // is used on its own stream only), and a CUDA graph that captured the plan keeps reading live
+  // metadata. Otherwise new storage is allocated and the old freed after the commit.
+  int32_t* d = nullptr;
+  const bool fresh = !(p->dev && p->dev_cap >= bytes);
+  if (fresh) {
+    if (cudaMallocAsync((void**)&d, bytes, stream) != cudaSuccess) return PG_ERR_CUDA;
+  } else {
+    d = p->dev;
+  }
+  if (cudaMemcpyAsync(d, st.host[k], bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaEventRecord(st.done[k], stream) != cudaSuccess) {
+    if (fresh) cudaFreeAsync(d, stream);
+    return PG_ERR_CUDA;
+  }
+  st.next = k ^ 1;
 
   q.num_req = num_req; q.num_tokens = T; q.num_qo_heads = Hq; q.num_kv_heads = Hkv;
   q.head_dim = D; q.page_size = ps;
@@ -270,11 +329,13 @@ int build_plan(pg_plan* p, int32_t num_req, const int64_t* qo_indptr,
   q.num_work = (int32_t)nwork; q.num_pairs = (int32_t)(ptab.size() / 8); q.num_page_ids = NP;
   q.stream = stream; q.device = dev;
   q.dev = d; q.dev_elems = host.size();
+  q.dev_cap = fresh ? bytes : p->dev_cap;
 
   // Commit: only now does the caller's plan change.
   int32_t* old = p->dev;
+  q.stage = p->stage;
   *p = q;
-  if (old) cudaFreeAsync(old, stream);
+  if (fresh && old) cudaFreeAsync(old, stream);
   return PG_OK;
 }
 
@@ -503,6 +564,7 @@ int pg_plan_paged_prefill(pg_plan_t* plan, int32_t num_req, const int64_t* qo_in
   int rc = build_plan(p, num_req, qo_indptr, kv_page_indptr, page_ids, last_page_len, start_pos,
                       num_qo_heads, num_kv_heads, head_dim, page_size, s);
   if (rc != PG_OK) {
+    free_stage(&p->stage);
     delete p;
     return rc;
   }
@@ -528,6 +590,7 @@ int pg_plan_paged_prefill_ring(pg_plan_t* plan, int32_t num_req, const int64_t* 
   int rc = build_plan(p, num_req, qo_indptr, kv_page_indptr, page_ids, nullptr, start_pos,
                       num_qo_heads, num_kv_heads, head_dim, page_size, s, window_left);
   if (rc != PG_OK) {
+    free_stage(&p->stage);
     delete p;
     return rc;
   }
@@ -555,6 +618,7 @@ int pg_plan_paged_segment(pg_plan_t* plan, int32_t num_req, const int64_t* qo_in
   int rc = build_plan(p, num_req, qo_indptr, kv_page_indptr, page_ids, last_page_len, start_pos,
                       num_qo_heads, num_kv_heads, head_dim, page_size, s, -1, ks);
   if (rc != PG_OK) {
+    free_stage(&p->stage);
     delete p;
     return rc;
   }
@@ -565,6 +629,7 @@ int pg_plan_paged_segment(pg_plan_t* plan, int32_t num_req, const int64_t* qo_in
 void pg_plan_destroy(pg_plan_t plan) {
   if (!plan) return;
   if (plan->dev) cudaFreeAsync(plan->dev, plan->stream);
+  free_stage(&plan->stage);
   delete plan;
 }
 
