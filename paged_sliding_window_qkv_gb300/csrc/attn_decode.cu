@@ -22,16 +22,21 @@
 //              then). Page ids are resolved 32 boxes at a time, one per lane, each checked
 //              against the plan and the pool (a bad id marks the unit skipped and sets the
 //              status word; nothing is read through it).
-//   warps 0..NW-1  consumers, one per 128 output columns: S = Q K^T partial over the warp's 128 d
-//              on bf16 mma.sync, partial S exchanged through shared memory (an mbarrier per
-//              buffer, every wait bounded), the sum taken in one fixed order by every warp (so
-//              every warp holds the same S, maximum and weights), online softmax in log2 units,
-//              O += P V for the warp's columns, then the segment's output or record.
+//   consumers, in one of two forms:
+//     group up to 4: one warp takes whole units with the products transposed (S^T = K Q^T,
+//              O^T = V^T P^T on bf16 mma.sync): the unit's 16 keys, and then 16 output columns at
+//              a time, are the MMA rows and the group's query rows are the 8 MMA columns, so no
+//              MMA row is padding and no partial sums cross warps;
+//     larger groups: NW = D / 128 warps, one per 128 output columns: S = Q K^T partial over the
+//              warp's 128 d, partial S exchanged through shared memory (an mbarrier per buffer),
+//              the sum taken in one fixed order by every warp (so every warp holds the same S,
+//              maximum and weights), O += P V for the warp's columns.
+//   Both run the online softmax in log2 units and end a segment with its output or record.
 // Decode is bound by HBM: per unit the CTA moves 16 K and 16 V rows of one head (16 KB at
 // head_dim 256, 32 KB at 512) and does 4 * 16 * G * D flop on them. A unit's consumer work is a
-// chain of dependent steps (partial S, exchange, softmax, PV), so what keeps HBM busy is the
-// number of units in flight per SM: the rings are short (3 stages at head_dim 256, 2 at 512)
-// so that 3 or 2 CTAs share each SM, each with its own producer and consumers.
+// chain of dependent steps, so what keeps HBM busy is the number of units in flight per SM: the
+// rings are short (3 stages at head_dim 256, 2 at 512) so that 4 (transposed form), 3 or 2
+// CTAs share each SM, each with its own producer and consumers.
 //
 // Every wait is bounded (two seconds of %globaltimer unless the launch passes a shorter limit);
 // a wait that runs out sets the device status word and the CTA leaves its loop; a producer that
@@ -48,7 +53,7 @@ namespace pg {
 namespace {
 
 constexpr int kUnit = 16;                      // keys per unit
-constexpr int kMaxDecodeCtas = 456;            // records are sized for this many CTAs (3 per SM)
+constexpr int kMaxDecodeCtas = 608;            // records are sized for this many CTAs (4 per SM)
 constexpr float kLn2 = 0.69314718055994531f;
 
 // unit header flags
@@ -58,20 +63,26 @@ constexpr int kSplit = 4;   // the segment also has units in another CTA: write 
 constexpr int kBad = 8;     // out-of-range metadata: the unit was not loaded, skip it
 constexpr int kEnd = 16;    // the CTA's last unit
 
-template <int D>
+// TR selects the consumer form. false: NW = D / 128 warps share each unit, warp w owning
+// columns [128w, 128w + 128) (any group up to 16). true (group up to 4): one warp takes whole
+// units with the products transposed, S^T = K Q^T and O^T = V^T P^T, so the keys and the output
+// columns fill the 16 MMA rows and the group sits in the 8 MMA columns; with a small Q region
+// the CTA fits 4 to an SM.
+template <int D, bool TR>
 struct DecCfg {
-  static constexpr int NW = D / 128;             // consumer warps; warp w owns columns [128w, 128w+128)
+  static constexpr int NW = TR ? 1 : D / 128;    // consumer warps
   static constexpr int NC = D / 64;              // 128-byte chunks of one row
   static constexpr int THREADS = (NW + 1) * 32;
   static constexpr int HALF = kUnit * D * 2;     // K (or V) bytes of one unit
   static constexpr int STAGE = 2 * HALF;         // K, then V
   static constexpr int NS = D == 256 ? 3 : 2;    // stages
-  static constexpr int MIN_CTAS = D == 256 ? 3 : 2;  // CTAs per SM
-  // Q slots share 32 rows of D: NQ = 32 / G slots of G rows each (2 to 8 slots); MMA rows past
-  // the group read one zero row
-  static constexpr int QBYTES = 32 * D * 2;
+  static constexpr int MIN_CTAS = TR ? 4 : D == 256 ? 3 : 2;  // CTAs per SM
+  // Q slots share QROWS rows of D: NQ = QROWS / G slots of G rows each (a power of two, 2 to 8
+  // slots); MMA rows (or columns) past the group read one zero row
+  static constexpr int QROWS = TR ? 8 : 32;
+  static constexpr int QBYTES = QROWS * D * 2;
   static constexpr int NQMAX = 8;
-  static constexpr int XBUF = NW * 32 * 8 * 4;   // partial S of every consumer warp
+  static constexpr int XBUF = TR ? 0 : NW * 32 * 8 * 4;  // partial S of every consumer warp
   static constexpr int OFF_Q = NS * STAGE;
   static constexpr int OFF_ZROW = OFF_Q + QBYTES;  // one row of D zeros
   static constexpr int OFF_X = OFF_ZROW + D * 2;
@@ -105,6 +116,7 @@ struct DecArgs {
   int64_t* prefix;           // [R + 1] units before request r (all heads); [R] = U
   int32_t num_qo_heads, num_kv_heads, group, page_size, num_pages, window_left;
   int32_t box_rows;          // key rows per TMA box: min(page_size, 16)
+  int32_t box_lg, page_lg;   // log2 of box_rows and of page_size (both powers of two)
   float scale_log2;
   int* status;
   uint64_t wait_ns;
@@ -203,10 +215,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Byte offset in a unit's K or V half of 16-byte piece u (0..7) of chunk c of key row k: the
 // unit lands as 16 / box_rows boxes, each [chunk][box_rows rows][128 B] with the 128-byte
-// swizzle (piece index XOR the row's 128-byte line index within the 1024-byte-aligned stage).
+// swizzle (piece index XOR the row's 128-byte line index within the 1024-byte-aligned stage);
+// box_rows br is a power of two.
 template <int NC>
 __device__ __forceinline__ uint32_t kv_off(int k, int c, int u, int br) {
-  const uint32_t row = (uint32_t)((k / br) * (br * NC * 128) + c * (br * 128) + (k % br) * 128);
+  const int lo = k & (br - 1);
+  const uint32_t row = (uint32_t)((k - lo) * (NC * 128) + c * (br * 128) + lo * 128);
   return row + (uint32_t)((u ^ ((row >> 7) & 7)) << 4);
 }
 
@@ -238,10 +252,10 @@ __device__ __forceinline__ ReqUnits req_units(const DecArgs& a, int32_t r) {
   return u;
 }
 
-template <int D>
-__global__ void __launch_bounds__(DecCfg<D>::THREADS, DecCfg<D>::MIN_CTAS)
+template <int D, bool TR>
+__global__ void __launch_bounds__(DecCfg<D, TR>::THREADS, DecCfg<D, TR>::MIN_CTAS)
 attn_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecArgs a) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, TR>;
   constexpr int NW = C::NW, NS = C::NS, NC = C::NC;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -259,7 +273,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecArgs a) {
   const int32_t G = a.group, Hq = a.num_qo_heads, Hkv = a.num_kv_heads;
   // Q slots: G rows each, a power of two of them (2 to 8) in the Q region
   const int32_t qslot = G * D * 2;
-  const int32_t lnq = (32 / G) >= 8 ? 3 : (32 / G) >= 4 ? 2 : 1;
+  const int32_t lnq = (C::QROWS / G) >= 8 ? 3 : (C::QROWS / G) >= 4 ? 2 : 1;
   const int32_t NQ = 1 << lnq;
 
   if (threadIdx.x == 0) {
@@ -286,19 +300,36 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecArgs a) {
     // ------------------------------------------------------------ producer
     const int32_t R = a.plan.num_req;
     const int32_t S = (int32_t)gridDim.x, s = (int32_t)blockIdx.x;
-    // units of every request (all heads), a warp-wide scan 32 requests at a time: the total U;
-    // CTA 0 also stores the prefix for the merge kernel
-    int64_t run = 0;
-    for (int32_t c = 0; c < R; c += 32) {
-      const int32_t r = c + lane;
-      const int64_t v = r < R ? (int64_t)req_units(a, r).n * Hkv : 0;
+    // Units of every request (all heads), in warp-wide scans of 32 requests: the total U, and
+    // (CTA 0) the prefix for the merge kernel. The first kHeld chunks' counts are loaded at
+    // once (one round trip to memory) and stay in registers for the second scan.
+    constexpr int kHeld = 8;
+    auto units_of = [&](int32_t r) -> int64_t { return r < R ? (int64_t)req_units(a, r).n * Hkv : 0; };
+    auto scan32 = [&](int64_t v) {  // inclusive prefix over the warp
       int64_t incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      if (s == 0 && r < R) a.prefix[r] = run + incl - v;
+      return incl;
+    };
+    int64_t held[kHeld];
+#pragma unroll
+    for (int j = 0; j < kHeld; ++j) held[j] = units_of(32 * j + lane);
+    int64_t run = 0;
+#pragma unroll
+    for (int j = 0; j < kHeld; ++j) {
+      if (32 * j < R) {
+        const int64_t incl = scan32(held[j]);
+        if (s == 0 && 32 * j + lane < R) a.prefix[32 * j + lane] = run + incl - held[j];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    for (int32_t c = 32 * kHeld; c < R; c += 32) {
+      const int64_t v = units_of(c + lane);
+      const int64_t incl = scan32(v);
+      if (s == 0 && c + lane < R) a.prefix[c + lane] = run + incl - v;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     const int64_t U = run;
@@ -308,27 +339,38 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecArgs a) {
     int32_t r = 0;
     int64_t rbase = 0;
     run = 0;
-    for (int32_t c = 0; c < R; c += 32) {
-      const int32_t rr = c + lane;
-      const int64_t v = rr < R ? (int64_t)req_units(a, rr).n * Hkv : 0;
-      int64_t incl = v;
+    bool found = false;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+    for (int j = 0; j < kHeld; ++j) {
+      if (!found && 32 * j < R) {
+        const int64_t incl = scan32(held[j]);
+        const uint32_t past = __ballot_sync(0xffffffffu, run + incl > u0);
+        if (past) {
+          const int f = __ffs(past) - 1;
+          r = 32 * j + f;
+          rbase = run + __shfl_sync(0xffffffffu, incl - held[j], f);
+          found = true;
+        } else {
+          run += __shfl_sync(0xffffffffu, incl, 31);
+        }
       }
+    }
+    for (int32_t c = 32 * kHeld; !found && c < R; c += 32) {
+      const int64_t v = units_of(c + lane);
+      const int64_t incl = scan32(v);
       const uint32_t past = __ballot_sync(0xffffffffu, run + incl > u0);
       if (past) {
         const int f = __ffs(past) - 1;
         r = c + f;
         rbase = run + __shfl_sync(0xffffffffu, incl - v, f);
-        break;
+        found = true;
+      } else {
+        run += __shfl_sync(0xffffffffu, incl, 31);
       }
-      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    const int32_t ps = a.page_size, BR = a.box_rows, NB = kUnit / BR;  // boxes per unit
+    const int32_t ps = a.page_size, BR = a.box_rows, LNB = 4 - a.box_lg, NB = 1 << LNB;  // boxes per unit
     const uint32_t box_bytes = (uint32_t)BR * D * 2;
-    const int32_t UB = 32 / NB;  // units per lookup batch
+    const int32_t UB = 32 >> LNB;  // units per lookup batch
     int64_t u = u0;
     int32_t i = 0;     // units issued by this CTA
     int32_t nseg = 0;  // segments started by this CTA
@@ -370,22 +412,22 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecArgs a) {
       for (int64_t ub = u; ok && ub < stop; ub += UB) {
         // lane l resolves box l % NB of unit ub + l / NB: its page id (or -1 past the keys held,
         // or num_pages when the metadata is out of range)
-        const int32_t jl = (int32_t)(ub - seg0) + lane / NB;  // unit within the segment
-        const int32_t rel = (q.j0 + jl) * kUnit + (lane % NB) * BR;  // key index among those held
+        const int32_t jl = (int32_t)(ub - seg0) + (lane >> LNB);  // unit within the segment
+        const int32_t rel = (q.j0 + jl) * kUnit + (lane & (NB - 1)) * BR;  // key index among those held
         int32_t page = -1, row = 0;
-        if (ub + lane / NB < stop && q.ks0 + rel < q.kv_len) {
-          const int32_t lp = rel / ps;
+        if (ub + (lane >> LNB) < stop && q.ks0 + rel < q.kv_len) {
+          const int32_t lp = rel >> a.page_lg;
           const int32_t pidx = q.kvp0 + (a.plan.ring ? lp % max(npg, 1) : lp);
           page = (pidx < q.kvp1 && pidx < a.plan.num_page_ids) ? a.plan.page_ids[pidx] : a.num_pages;
           if (page < 0 || page >= a.num_pages) page = a.num_pages;
-          else row = ((page * 2) * Hkv + g) * ps + rel % ps;  // K row; V is Hkv * ps rows later
+          else row = ((page * 2) * Hkv + g) * ps + (rel & (ps - 1));  // K row; V is Hkv * ps rows later
         }
         const int32_t nb_units = (int32_t)(stop - ub < UB ? stop - ub : UB);
         for (int32_t t = 0; t < nb_units; ++t, ++i) {
           const int st = i % NS;
           const int32_t jj = (int32_t)(ub - seg0) + t;
           const int32_t k0 = q.ks0 + (q.j0 + jj) * kUnit;
-          const bool lane_box = lane / NB == t;
+          const bool lane_box = (lane >> LNB) == t;
           const bool bad = __any_sync(0xffffffffu, lane_box && page == a.num_pages);
           const uint32_t nload = __popc(__ballot_sync(0xffffffffu, lane_box && page >= 0 &&
                                                                        page < a.num_pages));
@@ -419,7 +461,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecArgs a) {
             break;
           }
           if (!bad && lane_box && page >= 0 && page < a.num_pages) {
-            const uint32_t dst = base + st * C::STAGE + (lane % NB) * box_bytes;
+            const uint32_t dst = base + st * C::STAGE + (lane & (NB - 1)) * box_bytes;
             tma_3d(dst, &tm_kv, 0, row, 0, FULL(st));                      // K rows
             tma_3d(dst + C::HALF, &tm_kv, 0, row + Hkv * ps, 0, FULL(st));  // V rows
           }
@@ -439,6 +481,182 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecArgs a) {
       const uint64_t t0 = gtimer();
       while (gtimer() - t0 < 100000ull) {
       }
+    }
+  } else if constexpr (TR) {
+    // ------------------------------------------------------------ consumer (whole units)
+    // Fragments (m16n8k16): S^T = K Q^T has the unit's 16 keys as rows and the group's query
+    // rows as the 8 columns; lane (gid, tig) holds S of keys gid and gid + 8 for query rows 2 tig
+    // and 2 tig + 1. O^T = V^T P^T has output columns d as rows: o[mt] holds columns 16 mt + gid
+    // and 16 mt + gid + 8 for the same two query rows.
+    const int gid = lane >> 2, tig = lane & 3;
+    const int BR = a.box_rows;
+    float o[16][4];
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    uint32_t qf[16][2];
+    int32_t nseg = 0;
+    // P as the B operand: lane (gid, tig) needs query row gid at keys 2 tig, 2 tig + 1 (+ 8),
+    // which lanes 8 tig + gid / 2 and 8 tig + 4 + gid / 2 hold, in the half gid & 1
+    const int src0 = 8 * tig + (gid >> 1), src1 = src0 + 4;
+    const uint32_t psel = (gid & 1) ? 0x7632u : 0x5410u;
+    for (int32_t i = 0;; ++i) {
+      const int st = i % NS;
+      if (!bar_wait(FULL(st), (i / NS) & 1, wt)) break;
+      const DecUnit h = *reinterpret_cast<const DecUnit*>(gb + C::OFF_HDR + st * C::HDR);
+      if (h.flags & kFirst) {
+        const int qs = nseg & (NQ - 1);
+        if (!bar_wait(QFULL(qs), (nseg >> lnq) & 1, wt)) break;
+        // B fragments of Q^T over all D: query row lane & 7 (rows past the group read the zero
+        // row), four 8-wide pieces of d per load
+        const int qrow = lane & 7;
+        const uint32_t qb = qrow < G ? base + C::OFF_Q + qs * qslot + qrow * (D * 2)
+                                     : base + C::OFF_ZROW;
+#pragma unroll
+        for (int pq = 0; pq < D / 32; ++pq) {
+          uint32_t r4[4];
+          ldsm_x4(qb + (uint32_t)((32 * pq + 8 * (lane >> 3)) * 2), r4);
+          qf[2 * pq][0] = r4[0];
+          qf[2 * pq][1] = r4[1];
+          qf[2 * pq + 1][0] = r4[2];
+          qf[2 * pq + 1][1] = r4[3];
+        }
+        ++nseg;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+      }
+      const uint32_t kb = base + st * C::STAGE, vb = kb + C::HALF;
+      if (!(h.flags & kBad)) {
+        // ---- S^T over all D in 16 k-steps, four independent accumulator chains
+        float sa[4][4] = {};
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t kf[8][4];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int ks = 8 * hb + j;
+            ldsm_x4(kb + kv_off<NC>(lane & 15, ks >> 2, 2 * (ks & 3) + (lane >> 4), BR), kf[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            mma_bf16(sa[j & 3], kf[j], qf[8 * hb + j][0], qf[8 * hb + j][1]);
+        }
+        // ---- mask, scale (log2 units), online softmax per query row (a column here); element
+        // e is key k0 + gid + 8 (e >> 1) of query row 2 tig + (e & 1)
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float sv = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
+          const int32_t key = h.k0 + gid + 8 * (e >> 1);
+          t[e] = (key >= h.klo && key < h.khi) ? sv * a.scale_log2 : -INFINITY;
+        }
+        float mx0 = fmaxf(t[0], t[2]), mx1 = fmaxf(t[1], t[3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float n0 = fmaxf(m[0], mx0), n1 = fmaxf(m[1], mx1);
+        // a row that has seen no visible key yet keeps weight 0 (reference 0, not -inf)
+        const float r0 = n0 == -INFINITY ? 0.f : n0, r1 = n1 == -INFINITY ? 0.f : n1;
+        const float al0 = ex2(m[0] - r0), al1 = ex2(m[1] - r1);
+        m[0] = n0;
+        m[1] = n1;
+        const uint32_t plo = pack_bf16(ex2(t[0] - r0), ex2(t[1] - r1));  // key gid
+        const uint32_t phi = pack_bf16(ex2(t[2] - r0), ex2(t[3] - r1));  // key gid + 8
+        // the row sums add the bf16-rounded weights the PV product uses (this lane's two keys;
+        // summed over the lanes at the segment's end)
+        auto lo16 = [](uint32_t v) { return __uint_as_float(v << 16); };
+        auto hi16 = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
+        l[0] = l[0] * al0 + (lo16(plo) + lo16(phi));
+        l[1] = l[1] * al1 + (hi16(plo) + hi16(phi));
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            o[n][0] *= al0; o[n][1] *= al1;
+            o[n][2] *= al0; o[n][3] *= al1;
+          }
+        }
+        const uint32_t pb0 = __byte_perm(__shfl_sync(0xffffffffu, plo, src0),
+                                         __shfl_sync(0xffffffffu, plo, src1), psel);
+        const uint32_t pb1 = __byte_perm(__shfl_sync(0xffffffffu, phi, src0),
+                                         __shfl_sync(0xffffffffu, phi, src1), psel);
+        // V rows past the keys the request holds may be anything: they read as zero
+        if (h.vz < kUnit) {
+          for (int idx = lane; idx < (kUnit - h.vz) * NC * 8; idx += 32) {
+            const int k = h.vz + idx / (NC * 8);
+            *reinterpret_cast<uint4*>(gb + (vb - base) + kv_off<NC>(k, (idx >> 3) % NC, idx & 7, BR)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+        }
+        // ---- O^T += V^T P^T: 16 row tiles of 16 output columns, one k-step of 16 keys
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t vf[8][4];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int mt = 8 * hb + j;
+            ldsm_x4_t(vb + kv_off<NC>((lane & 7) + 8 * (lane >> 4), mt >> 2,
+                                      2 * (mt & 3) + ((lane >> 3) & 1), BR),
+                      vf[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mma_bf16(o[8 * hb + j], vf[j], pb0, pb1);
+        }
+        if (h.vz < kUnit) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      if (h.flags & kLast) {
+        // ---- the segment's output (or this CTA's record of it): query rows 2 tig + j < G
+        float lt[2] = {l[0], l[1]};
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          lt[0] += __shfl_xor_sync(0xffffffffu, lt[0], off);
+          lt[1] += __shfl_xor_sync(0xffffffffu, lt[1], off);
+        }
+        const float iv[2] = {lt[0] > 0.f ? 1.f / lt[0] : 0.f, lt[1] > 0.f ? 1.f / lt[1] : 0.f};
+        if (h.flags & kSplit) {
+          const int64_t rb = ((int64_t)blockIdx.x * 2 + h.rec) * G;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int row = 2 * tig + j;
+            if (row < G) {
+              float* dst = a.rec_o + (rb + row) * D + gid;
+#pragma unroll
+              for (int n = 0; n < 16; ++n) {
+                dst[16 * n] = o[n][j] * iv[j];
+                dst[16 * n + 8] = o[n][2 + j] * iv[j];
+              }
+              if (gid == 0)
+                *reinterpret_cast<float2*>(a.rec_ml + (rb + row) * 2) = make_float2(m[j], lt[j]);
+            }
+          }
+        } else {
+          const int32_t tok = a.plan.qo_indptr[h.r];
+          const int64_t row0 = (int64_t)tok * Hq + (int64_t)h.g * G;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int row = 2 * tig + j;
+            if (row < G) {
+              __nv_bfloat16* dst = a.out + (row0 + row) * D + gid;
+#pragma unroll
+              for (int n = 0; n < 16; ++n) {
+                dst[16 * n] = __float2bfloat16_rn(o[n][j] * iv[j]);
+                dst[16 * n + 8] = __float2bfloat16_rn(o[n][2 + j] * iv[j]);
+              }
+              if (a.lse && gid == 0)
+                a.lse[row0 + row] = lt[j] > 0.f ? (m[j] + log2f(lt[j])) * kLn2 : -INFINITY;
+            }
+          }
+        }
+      }
+      // the stage (and its header) is released only now; at the segment's end so is its Q slot
+      __syncwarp();
+      if (lane == 0) {
+        bar_arrive(EMPTY(st));
+        if (h.flags & kLast) bar_arrive(QEMPTY((nseg - 1) & (NQ - 1)));
+      }
+      if (h.flags & kEnd) break;
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -614,12 +832,16 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecArgs a) {
 
 // Combine the records of each segment cut by CTA range boundaries, write the rows of segments
 // that see no key (out = 0, lse = -inf); segments inside one CTA's range were written directly.
-// One CTA per (request, KV head).
+// One CTA per (request, KV head). The request's entry and the unit prefixes are loaded together,
+// then each thread loads the (m, l) and columns of up to four records at once and folds them
+// in with a running maximum: about two round trips to memory per segment.
 template <int D>
 __global__ void __launch_bounds__(128) attn_decode_merge_kernel(DecArgs a, int32_t S) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t Hkv = a.num_kv_heads, G = a.group, Hq = a.num_qo_heads;
   const int32_t r = (int32_t)blockIdx.x / Hkv, g = (int32_t)blockIdx.x % Hkv;
+  const int64_t U = a.prefix[a.plan.num_req];
+  const int64_t pre = a.prefix[r];
   const ReqUnits q = req_units(a, r);
   const int64_t row0 = (int64_t)q.tok * Hq + (int64_t)g * G;
   if (q.n == 0) {
@@ -628,31 +850,40 @@ __global__ void __launch_bounds__(128) attn_decode_merge_kernel(DecArgs a, int32
     if (a.lse && (int)threadIdx.x < G) a.lse[row0 + threadIdx.x] = -INFINITY;
     return;
   }
-  const int64_t U = a.prefix[a.plan.num_req];  // > 0: this request has units
-  const int64_t first = (int64_t)a.prefix[r] + (int64_t)g * q.n, last = first + q.n - 1;
+  const int64_t first = pre + (int64_t)g * q.n, last = first + q.n - 1;  // U > 0 here
   auto cta_of = [&](int64_t x) { return (int32_t)(((x + 1) * S - 1) / U); };
   const int32_t sa = cta_of(first), sb = cta_of(last);
   if (sa == sb) return;
   // the record slot of CTA s: a segment that started before CTA s's range is its first (slot 0);
   // in CTA sa the segment is the first only when the range starts inside it
-  auto slot = [&](int32_t s) { return (s == sa && (int64_t)s * U / S < first) ? 1 : 0; };
-  // CTAs with an empty range (more CTAs than units) hold no record
-  auto holds = [&](int32_t s) { return (int64_t)s * U / S < (int64_t)(s + 1) * U / S; };
+  const int32_t slot_a = (int64_t)sa * U / S < first ? 1 : 0;
   for (int idx = threadIdx.x; idx < G * (D / 4); idx += blockDim.x) {
     const int row = idx / (D / 4), c4 = idx % (D / 4);
-    float M = -INFINITY;
-    for (int32_t s = sa; s <= sb; ++s)
-      if (holds(s)) M = fmaxf(M, a.rec_ml[(((int64_t)s * 2 + slot(s)) * G + row) * 2]);
-    float den = 0.f;
+    float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int32_t s = sa; s <= sb; ++s) {
-      if (!holds(s)) continue;
-      const int64_t rb = ((int64_t)s * 2 + slot(s)) * G + row;
-      const float2 ml = *reinterpret_cast<const float2*>(a.rec_ml + rb * 2);
-      const float wgt = ml.y > 0.f ? ml.y * exp2f(ml.x - M) : 0.f;
-      const float4 v = *reinterpret_cast<const float4*>(a.rec_o + rb * D + 4 * c4);
-      acc.x += wgt * v.x; acc.y += wgt * v.y; acc.z += wgt * v.z; acc.w += wgt * v.w;
-      den += wgt;
+    for (int32_t s0 = sa; s0 <= sb; s0 += 4) {
+      float2 ml[4];
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int32_t s = s0 + k;
+        // CTAs with an empty range (more CTAs than units) hold no record
+        const bool holds = s <= sb && (int64_t)s * U / S < (int64_t)(s + 1) * U / S;
+        const int64_t rb = ((int64_t)s * 2 + (s == sa ? slot_a : 0)) * G + row;
+        ml[k] = holds ? *reinterpret_cast<const float2*>(a.rec_ml + rb * 2) : make_float2(-INFINITY, 0.f);
+        v[k] = holds ? *reinterpret_cast<const float4*>(a.rec_o + rb * D + 4 * c4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (!(ml[k].y > 0.f)) continue;
+        const float mn = fmaxf(M, ml[k].x);
+        const float so = exp2f(M - mn), w = ml[k].y * exp2f(ml[k].x - mn);  // M = -inf: so = 0
+        acc.x = acc.x * so + w * v[k].x; acc.y = acc.y * so + w * v[k].y;
+        acc.z = acc.z * so + w * v[k].z; acc.w = acc.w * so + w * v[k].w;
+        den = den * so + w;
+        M = mn;
+      }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     __nv_bfloat16* dst = a.out + (row0 + row) * D + 4 * c4;
@@ -683,9 +914,9 @@ EncodeTiledFn encode_fn_dec() {
 
 size_t align16(size_t n) { return (n + 15) & ~(size_t)15; }
 
-template <int D>
+template <int D, bool TR>
 cudaError_t launch_dec(const AttnArgs& a, cudaStream_t stream) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, TR>;
   EncodeTiledFn enc = encode_fn_dec();
   if (!enc) return cudaErrorNotSupported;
   const int32_t ps = a.pool.page_size, Hkv = a.pool.num_kv_heads, G = a.group;
@@ -720,6 +951,8 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t stream) {
   d.num_pages = a.pool.num_pages;
   d.window_left = a.window_left;
   d.box_rows = br;
+  d.box_lg = 31 - __builtin_clz((unsigned)br);
+  d.page_lg = 31 - __builtin_clz((unsigned)ps);
   d.scale_log2 = a.sm_scale_log2;
   d.status = a.status;
   d.wait_ns = a.wait_ns;
@@ -729,13 +962,13 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = setup.get(dev, [dev](int* n) {
-    cudaError_t rr = cudaFuncSetAttribute(attn_decode_kernel<D>,
+    cudaError_t rr = cudaFuncSetAttribute(attn_decode_kernel<D, TR>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (rr != cudaSuccess) return rr;
     int sms = 0, per = 0;
     rr = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (rr != cudaSuccess) return rr;
-    rr = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_decode_kernel<D>, C::THREADS,
+    rr = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_decode_kernel<D, TR>, C::THREADS,
                                                        C::SMEM);
     if (rr != cudaSuccess) return rr;
     *n = std::max(1, sms * std::max(per, 1));
@@ -744,7 +977,7 @@ cudaError_t launch_dec(const AttnArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   // one persistent CTA per slot; CTAs beyond the step's units run an empty range
   const int32_t grid = std::min(slots, kMaxDecodeCtas);
-  attn_decode_kernel<D><<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(tm, d);
+  attn_decode_kernel<D, TR><<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(tm, d);
   count_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -787,7 +1020,9 @@ size_t attn_decode_stream_ws_bytes(int32_t num_req, int32_t group, int32_t head_
 
 cudaError_t launch_attn_decode_stream(const AttnArgs& a, int32_t head_dim, cudaStream_t stream) {
   if (a.plan.num_req == 0) return cudaSuccess;
-  return head_dim == 256 ? launch_dec<256>(a, stream) : launch_dec<512>(a, stream);
+  if (head_dim == 256)
+    return a.group <= 4 ? launch_dec<256, true>(a, stream) : launch_dec<256, false>(a, stream);
+  return launch_dec<512, false>(a, stream);
 }
 
 }  // namespace pg

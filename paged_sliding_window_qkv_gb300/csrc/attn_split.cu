@@ -401,9 +401,14 @@ attn_split_kernel(AttnArgs a) {
 
 // Combine the decode chunks of one (request, query head) row:
 // o = sum_c l_c 2^(m_c - M) o_c / sum_c l_c 2^(m_c - M).
+// The chunks' (m, l) pairs are loaded once, spread over the threads, and kept in shared memory
+// (256 chunks at a time); then each thread issues its loads of four columns for eight chunks at
+// once, so a row waits for about two round trips to memory rather than one per chunk.
 template <int D>
 __global__ void __launch_bounds__(D / 4)
 attn_merge_kernel(AttnArgs a) {
+  constexpr int NT = D / 4, NWARP = NT / 32, CB = 256;
+  __shared__ float s_m[CB], s_l[CB], s_part[NWARP];
   const int32_t r = blockIdx.x, h = blockIdx.y;
   const PlanDev& pl = a.plan;
   const int32_t kvp0 = pl.kv_page_indptr[r], kvp1 = pl.kv_page_indptr[r + 1];
@@ -417,20 +422,56 @@ attn_merge_kernel(AttnArgs a) {
   const int32_t nch = (hi - lo + a.kv_chunk - 1) / a.kv_chunk;
   if (nch <= 1) return;  // written directly by the partition kernel
   const int64_t row = ((int64_t)r * a.num_qo_heads + h) * a.max_chunks;
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, a.ws_ml[(row + c) * 2]);
-  float den = 0.f;
+  const int tid = threadIdx.x, lane = tid & 31;
+  // the maximum M over the chunks
+  float mx = -INFINITY;
+  for (int c = tid; c < nch; c += NT) {
+    const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + (row + c) * 2);
+    mx = fmaxf(mx, ml.x);
+    if (c < CB) {
+      s_m[c] = ml.x;
+      s_l[c] = ml.y;
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) s_part[tid >> 5] = mx;
+  __syncthreads();
+  float M = s_part[0];
+  for (int wv = 1; wv < NWARP; ++wv) M = fmaxf(M, s_part[wv]);
+  const float Mr = M == -INFINITY ? 0.f : M;
+  // every thread sums the same weights in the same order, so all hold the same denominator
+  const int d = tid * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int d = threadIdx.x * 4;
-  for (int c = 0; c < nch; ++c) {
-    const float m = a.ws_ml[(row + c) * 2], l = a.ws_ml[(row + c) * 2 + 1];
-    const float w = l * exp2f(m - (M == -INFINITY ? 0.f : M));
-    const float4 v = *reinterpret_cast<const float4*>(a.ws_o + (row + c) * D + d);
-    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-    den += w;
+  float den = 0.f;
+  for (int cb = 0; cb < nch; cb += CB) {
+    const int n = min(CB, nch - cb);
+    if (cb > 0) {
+      __syncthreads();  // the previous block's weights have been read
+      for (int c = tid; c < n; c += NT) {
+        const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + (row + cb + c) * 2);
+        s_m[c] = ml.x;
+        s_l[c] = ml.y;
+      }
+      __syncthreads();
+    }
+    for (int c = tid; c < n; c += NT) s_l[c] = s_l[c] > 0.f ? s_l[c] * exp2f(s_m[c] - Mr) : 0.f;
+    __syncthreads();
+    for (int c0 = 0; c0 < n; c0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = c0 + k < n ? *reinterpret_cast<const float4*>(a.ws_o + (row + cb + c0 + k) * D + d)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float w = c0 + k < n ? s_l[c0 + k] : 0.f;
+        acc.x += w * v[k].x; acc.y += w * v[k].y; acc.z += w * v[k].z; acc.w += w * v[k].w;
+        den += w;
+      }
+    }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  if (a.lse && threadIdx.x == 0)
+  if (a.lse && tid == 0)
     a.lse[(int64_t)pl.qo_indptr[r] * a.num_qo_heads + h] =
         den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
   __nv_bfloat16* dst = a.out + ((int64_t)pl.qo_indptr[r] * a.num_qo_heads + h) * D + d;

@@ -75,7 +75,7 @@ def test_page_sizes(fam, ps):
     parity.attn_gate(gpu, ref, f"{fam.name} page size {ps}")
 
 
-@pytest.mark.parametrize("hq,hkv,d", [(16, 16, 256), (16, 4, 256), (8, 1, 256),
+@pytest.mark.parametrize("hq,hkv,d", [(16, 16, 256), (16, 4, 256), (8, 1, 256), (16, 1, 256),
                                       (16, 16, 512), (4, 2, 512), (16, 1, 512)])
 def test_head_groupings(hq, hkv, d):
     fam = W.Family("x", hq, hkv, d, 1e4, -1)
