@@ -171,23 +171,36 @@ attn_split_kernel(AttnArgs a) {
   // and the TPK threads of a row move consecutive 16-byte chunks
   constexpr int TPK = kThreads / BN;  // threads per key row
   static_assert(kThreads % BN == 0 && C::CH % TPK == 0, "key-row copy split");
-  auto load_kv = [&](int stage, int32_t kb) {
-    const uint32_t bk = smem_u32(sK + stage * C::KV_BYTES);
-    const uint32_t bv = smem_u32(sV + stage * C::KV_BYTES);
-    const int jj = tid / TPK, c0 = tid % TPK;
+  // A tile's row copies are issued in two steps: the page lookup of the thread's row (a load
+  // of its page id, issued one tile ahead so that its latency overlaps a tile of compute), then
+  // the checks and the copies.
+  struct RowAt {
+    int32_t page, off;  // page id as loaded, row within the page; off < 0: no key of the request
+  };
+  const int jj = tid / TPK, c0 = tid % TPK;
+  auto row_fetch = [&](int32_t kb) {
+    RowAt r{-1, -1};
     const int32_t j = kb + jj;
-    bool valid = j < hi;
-    const __nv_bfloat16* src = a.pool.layer_base;
-    if (valid) {
+    if (j < hi) {
       const int32_t rel = j - ks0;  // index among the keys held
       const int32_t lp = rel / ps;  // logical page; ring addressing wraps it over the pages held
       const int32_t pidx = kvp0 + (pl.ring ? lp % max(kvp1 - kvp0, 1) : lp);
-      const int32_t page = pidx < kvp1 ? pl.page_ids[pidx] : -1;
-      if (page < 0 || page >= a.pool.num_pages) {
+      r.off = rel - lp * ps;
+      r.page = pidx < kvp1 ? pl.page_ids[pidx] : -1;
+    }
+    return r;
+  };
+  auto row_issue = [&](int stage, RowAt r) {
+    const uint32_t bk = smem_u32(sK + stage * C::KV_BYTES);
+    const uint32_t bv = smem_u32(sV + stage * C::KV_BYTES);
+    bool valid = r.off >= 0;
+    const __nv_bfloat16* src = a.pool.layer_base;
+    if (valid) {
+      if (r.page < 0 || r.page >= a.pool.num_pages) {
         if (c0 == 0) atomicOr(a.status, kStatusBounds);
         valid = false;
       } else {
-        src = kv_base + (int64_t)page * a.pool.stride_page + (int64_t)(rel % ps) * D;
+        src = kv_base + (int64_t)r.page * a.pool.stride_page + (int64_t)r.off * D;
       }
     }
 #pragma unroll
@@ -198,14 +211,18 @@ attn_split_kernel(AttnArgs a) {
   };
 
   const int32_t ntiles = (hi - lo + BN - 1) / BN;
-  // the first NS - 1 tiles (one commit group each; Q rides in the first)
-  load_kv(0, lo);
-  cp_async_commit();
+  // the first NS - 1 tiles (one commit group each; Q rides in the first), their lookups first
+  {
+    RowAt first[C::NS - 1];
 #pragma unroll
-  for (int st = 1; st < C::NS - 1; ++st) {
-    if (st < ntiles) load_kv(st, lo + st * BN);
-    cp_async_commit();
+    for (int st = 0; st < C::NS - 1; ++st) first[st] = row_fetch(lo + st * BN);
+#pragma unroll
+    for (int st = 0; st < C::NS - 1; ++st) {
+      if (st < ntiles) row_issue(st, first[st]);
+      cp_async_commit();
+    }
   }
+  RowAt pend = row_fetch(lo + (C::NS - 1) * BN);  // the tile the first iteration loads
 
   // S-warp coordinates
   const int s_mt = warp % C::WM;
@@ -232,8 +249,9 @@ attn_split_kernel(AttnArgs a) {
     // whose stage the next load reuses
     cp_async_wait<C::NS - 2>();
     __syncthreads();
-    if (it + C::NS - 1 < ntiles) load_kv((it + C::NS - 1) % C::NS, kb + (C::NS - 1) * BN);
+    if (it + C::NS - 1 < ntiles) row_issue((it + C::NS - 1) % C::NS, pend);
     cp_async_commit();
+    pend = row_fetch(kb + C::NS * BN);  // the next iteration's tile
 
     // ---- S = Q K^T (this warp: one m-tile, NT n-tiles, one k-split) ----
     {
@@ -482,9 +500,11 @@ attn_merge_kernel(AttnArgs a) {
 using Pre256 = Cfg<256, 64, 32, 2, 1, false>;
 using Pre512 = Cfg<512, 32, 32, 1, 1, false>;
 // decode streams K/V from HBM: three stages keep two tiles of loads in flight behind the one
-// being computed
+// being computed. At head_dim 512 a warp's S work is two key tiles over a quarter of d (two
+// independent MMA chains of 8 k-steps) rather than one key tile over half of d (one chain of
+// 16): the CTA is alone on its SM, so the chains' latency is what it waits on.
 using Dec256 = Cfg<256, 16, 32, 1, 2, true, 3>;
-using Dec512 = Cfg<512, 16, 32, 1, 2, true, 3>;
+using Dec512 = Cfg<512, 16, 32, 2, 4, true, 3>;
 
 template <class C>
 cudaError_t launch_split(const AttnArgs& a, dim3 grid, cudaStream_t stream) {
