@@ -241,6 +241,10 @@ attn_split_kernel(AttnArgs a) {
   float o[C::NTO][4];
 #pragma unroll
   for (int i = 0; i < C::NTO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  // a warp whose k-split spans at most 8 k-steps keeps its Q fragments in registers, loaded
+  // once the first commit group (Q and the first tile) has landed
+  constexpr bool kQReg = C::KSTEPS <= 8;
+  uint32_t qf[kQReg ? C::KSTEPS : 1][4];
 
   for (int32_t it = 0; it < ntiles; ++it) {
     const int stage = it % C::NS;
@@ -262,11 +266,22 @@ attn_split_kernel(AttnArgs a) {
       const uint32_t bk = smem_u32(sK + stage * C::KV_BYTES);
       const int qrow = s_mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
       const int n0 = s_ng * C::NT * 8;
-#pragma unroll 4
+      if constexpr (kQReg) {
+        if (it == 0) {
+#pragma unroll
+          for (int kk = 0; kk < C::KSTEPS; ++kk)
+            ldsm_x4(bq + swz<D>(qrow, (s_ks * C::KSTEPS + kk) * 2 + (lane >> 4)), qf[kk]);
+        }
+      }
+#pragma unroll(kQReg ? C::KSTEPS : 4)
       for (int kk = 0; kk < C::KSTEPS; ++kk) {
         const int kc = (s_ks * C::KSTEPS + kk) * 2;
         uint32_t af[4];
-        ldsm_x4(bq + swz<D>(qrow, kc + (lane >> 4)), af);
+        if constexpr (kQReg) {
+          af[0] = qf[kk][0]; af[1] = qf[kk][1]; af[2] = qf[kk][2]; af[3] = qf[kk][3];
+        } else {
+          ldsm_x4(bq + swz<D>(qrow, kc + (lane >> 4)), af);
+        }
         if (C::NT % 2 == 0) {
 #pragma unroll
           for (int nt = 0; nt < C::NT; nt += 2) {
@@ -300,7 +315,10 @@ attn_split_kernel(AttnArgs a) {
           for (int e = 0; e < 2; ++e) {
             const int col = n0 + nt * 8 + 2 * (lane & 3) + e;
             const int32_t j = kb + col;
-            const bool vis = rv && j < hi && j <= pos && (W < 0 || pos - j <= W);
+            // decode: every key in [lo, hi) is visible (the range already applies the window
+            // and hi <= position + 1)
+            const bool vis = C::DECODE ? rv && j < hi
+                                       : rv && j < hi && j <= pos && (W < 0 || pos - j <= W);
             S[m * C::SLD + col] = vis ? acc[nt][h2 * 2 + e] * a.sm_scale_log2 : -INFINITY;
           }
         }
