@@ -17,7 +17,8 @@
 //              (a page's rows of one KV head are contiguous; 128-byte swizzle, so the
 //              consumers' ldmatrix reads are conflict-free) into a ring of NS stages, with the
 //              unit's geometry in a stage header; each segment's Q rows (the G rows of its
-//              head group) by a bulk copy into one of NQ Q slots (8 at head_dim 256, 2 at 512),
+//              head group) by a bulk copy into one of NQ Q slots (2 to 8, as many as the Q
+//              region holds),
 //              which the consumers release when they finish the segment (a slot is read until
 //              then). Page ids are resolved 32 boxes at a time, one per lane, each checked
 //              against the plan and the pool (a bad id marks the unit skipped and sets the
