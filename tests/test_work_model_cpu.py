@@ -63,3 +63,26 @@ def test_decode_bytes_count_every_visible_row_once():
                 + b.num_req * f.num_qo_heads * f.head_dim * 2 * 2    # q in, out written
                 + (rows // b.page_size + b.num_req) * 4)             # page ids of the visible keys
         assert bench.decode_bytes(fi) == want
+
+
+def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch):
+    # a call's DRAM bytes come from the committed capture only while its kernel source hashes
+    # as recorded; any edit of the source (or a missing entry or file) gives None
+    import hashlib
+    import json
+    csrc = tmp_path / "paged_sliding_window_qkv_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = csrc / "k.cu"
+    src.write_bytes(b"kernel v1\n")
+    entry = {"case": "c", "source": "k.cu", "sha256": hashlib.sha256(b"kernel v1\n").hexdigest(),
+             "dram_bytes_per_launch": 12345, "scaled": 1}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"calls": {"call": entry}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_traffic("call") == 12345
+    assert bench.kernel_traffic("other call") is None
+    src.write_bytes(b"kernel v2\n")
+    assert bench.kernel_traffic("call") is None
+    src.unlink()
+    assert bench.kernel_traffic("call") is None
+
